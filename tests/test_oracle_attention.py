@@ -1,0 +1,283 @@
+"""Pins of the float64 attention oracle against things other than itself:
+hand-worked golden values, closed forms, invariants, brute force on tiny
+inputs and the ring == full-attention identity of the blockwise decomposition.
+"""
+import itertools
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import attention as OA
+from tests._golden import load, arr
+
+pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
+
+
+def _rand(rng, S, Hq, Hkv, d):
+    return rng.standard_normal((S, Hq, d)), rng.standard_normal((S, Hkv, d)), rng.standard_normal((S, Hkv, d))
+
+
+# ---------------------------------------------------------------- golden values
+
+def _golden_cases():
+    return load("attention_hand.json")["cases"]
+
+
+@pytest.mark.parametrize("case", _golden_cases(), ids=lambda c: c["name"])
+def test_full_attention_hand_worked(case):
+    O, LSE = oracle.full_attention(arr(case["q"]), arr(case["k"]), arr(case["v"]),
+                                   case["causal"], case["scale"])
+    np.testing.assert_allclose(O, arr(case["O"]), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(LSE, arr(case["LSE"]), rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("case", [c for c in _golden_cases() if len(c["q"]) % 2 == 0],
+                         ids=lambda c: c["name"])
+def test_ring_attention_hand_worked(case):
+    S = len(case["q"])
+    for N in [n for n in (1, 2, 4) if S % (2 * n) == 0]:
+        O, LSE = oracle.ring_attention(arr(case["q"]), arr(case["k"]), arr(case["v"]),
+                                       case["causal"], N, case["scale"])
+        np.testing.assert_allclose(O, arr(case["O"]), rtol=0, atol=1e-12)
+        np.testing.assert_allclose(LSE, arr(case["LSE"]), rtol=0, atol=1e-12)
+
+
+def _golden_all_pass():
+    for c in _golden_cases():
+        O, LSE = oracle.full_attention(arr(c["q"]), arr(c["k"]), arr(c["v"]), c["causal"], c["scale"])
+        if not (np.allclose(O, arr(c["O"]), atol=1e-9) and np.allclose(LSE, arr(c["LSE"]), atol=1e-9)):
+            return False
+    return True
+
+
+# planted mistakes (in the oracle, on the CPU) must be caught by the golden pins
+@pytest.mark.parametrize("mutation", ["gqa_mod", "mask_flipped", "mask_strict", "no_scale",
+                                      "log2_lse"])
+def test_planted_mistakes_are_caught(monkeypatch, mutation):
+    if mutation == "gqa_mod":
+        monkeypatch.setattr(OA, "_kv_head_of", lambda Hq, Hkv: np.arange(Hq) % Hkv)
+    elif mutation == "mask_flipped":
+        monkeypatch.setattr(OA, "_visible", lambda qp, kp: kp >= qp)
+    elif mutation == "mask_strict":
+        monkeypatch.setattr(OA, "_visible", lambda qp, kp: kp < qp)
+    elif mutation == "no_scale":
+        monkeypatch.setattr(OA, "_default_scale", lambda d, s: 1.0)
+    elif mutation == "log2_lse":
+        real = np.log
+        monkeypatch.setattr(OA.np, "log", lambda x: real(x) / math.log(2))
+    assert not _golden_all_pass()
+
+
+def test_planted_operand_swap_is_caught():
+    c = [c for c in _golden_cases() if c["name"] == "causal_three_tokens_direction_and_operand_order"][0]
+    # scores q_j.k_i instead of q_i.k_j: feed k as queries and q as keys
+    O, _ = oracle.full_attention(arr(c["k"]), arr(c["q"]), arr(c["v"]), True, 1.0)
+    assert not np.allclose(O, arr(c["O"]), atol=1e-6)
+
+
+# ---------------------------------------------------------------- brute force
+
+def _brute(q, k, v, causal, scale):
+    """Tiny-input brute force with math.exp and Python sums (no numpy algebra)."""
+    S, Hq, d = q.shape
+    Hkv = k.shape[1]
+    grp = Hq // Hkv
+    O = np.zeros(q.shape)
+    L = np.zeros((S, Hq))
+    for i in range(S):
+        for h in range(Hq):
+            g = h // grp
+            js = [j for j in range(S) if (j <= i or not causal)]
+            sc = [scale * sum(q[i, h, e] * k[j, g, e] for e in range(d)) for j in js]
+            mx = max(sc)
+            w = [math.exp(x - mx) for x in sc]
+            tot = sum(w)
+            for e in range(d):
+                O[i, h, e] = sum(wj * v[j, g, e] for wj, j in zip(w, js)) / tot
+            L[i, h] = mx + math.log(tot)
+    return O, L
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_full_attention_matches_brute_force(causal):
+    rng = np.random.default_rng(7)
+    q, k, v = _rand(rng, 6, 4, 2, 3)
+    O, L = oracle.full_attention(q, k, v, causal)
+    Ob, Lb = _brute(q, k, v, causal, 1 / math.sqrt(3))
+    np.testing.assert_allclose(O, Ob, atol=1e-12)
+    np.testing.assert_allclose(L, Lb, atol=1e-12)
+
+
+# ---------------------------------------------------------------- special cases, invariants
+
+def test_single_token_and_first_causal_row():
+    rng = np.random.default_rng(1)
+    q, k, v = _rand(rng, 5, 2, 2, 4)
+    O, L = oracle.full_attention(q, k, v, True)
+    np.testing.assert_allclose(O[0], v[0], atol=1e-15)
+    np.testing.assert_allclose(L[0], 0.5 * np.einsum("hd,hd->h", q[0], k[0]), atol=1e-14)
+
+
+def test_dominant_key():
+    rng = np.random.default_rng(2)
+    q, k, v = _rand(rng, 8, 1, 1, 4)
+    k[5] = 60.0 * q[0]        # overwhelms every other score for query 0
+    O, _ = oracle.full_attention(q[:1], k, v, False)
+    np.testing.assert_allclose(O[0, 0], v[5, 0], atol=1e-9)
+
+
+def test_key_order_invariance_non_causal():
+    rng = np.random.default_rng(3)
+    q, k, v = _rand(rng, 16, 2, 1, 8)
+    p = rng.permutation(16)
+    O1, L1 = oracle.full_attention(q, k, v, False)
+    O2, L2 = oracle.full_attention(q, k[p], v[p], False)
+    np.testing.assert_allclose(O1, O2, atol=1e-13)
+    np.testing.assert_allclose(L1, L2, atol=1e-13)
+
+
+def test_linearity_in_v():
+    rng = np.random.default_rng(4)
+    q, k, v1 = _rand(rng, 12, 2, 2, 4)
+    v2 = rng.standard_normal(v1.shape)
+    O1, _ = oracle.full_attention(q, k, v1, True)
+    O2, _ = oracle.full_attention(q, k, v2, True)
+    O3, _ = oracle.full_attention(q, k, 2.0 * v1 - 3.0 * v2, True)
+    np.testing.assert_allclose(O3, 2.0 * O1 - 3.0 * O2, atol=1e-12)
+
+
+def test_causal_rows_ignore_future_keys():
+    rng = np.random.default_rng(5)
+    q, k, v = _rand(rng, 10, 2, 1, 4)
+    O1, L1 = oracle.full_attention(q, k, v, True)
+    k2, v2 = k.copy(), v.copy()
+    k2[6:] = rng.standard_normal(k2[6:].shape)
+    v2[6:] = rng.standard_normal(v2[6:].shape)
+    O2, L2 = oracle.full_attention(q, k2, v2, True)
+    np.testing.assert_array_equal(O1[:6], O2[:6])
+    np.testing.assert_array_equal(L1[:6], L2[:6])
+    assert not np.allclose(O1[6:], O2[6:])
+
+
+def test_lse_bounds_and_convex_hull():
+    rng = np.random.default_rng(6)
+    q, k, v = _rand(rng, 9, 1, 1, 3)
+    O, L = oracle.full_attention(q, k, v, True)
+    for i in range(9):
+        s = (q[i, 0] @ k[: i + 1, 0].T) / math.sqrt(3)
+        assert s.max() - 1e-12 <= L[i, 0] <= s.max() + math.log(i + 1) + 1e-12
+        assert np.all(O[i, 0] >= v[: i + 1, 0].min(axis=0) - 1e-12)
+        assert np.all(O[i, 0] <= v[: i + 1, 0].max(axis=0) + 1e-12)
+
+
+def test_attention_rows_agrees_with_rows_of_full():
+    rng = np.random.default_rng(8)
+    q, k, v = _rand(rng, 20, 4, 2, 5)
+    O, L = oracle.full_attention(q, k, v, True, row_block=7)
+    rows = np.array([0, 3, 19, 7])
+    Or, Lr = oracle.attention_rows(q[rows], rows, k, v, True)
+    np.testing.assert_array_equal(Or, O[rows])
+    np.testing.assert_array_equal(Lr, L[rows])
+
+
+# ---------------------------------------------------------------- ring identity
+
+@pytest.mark.parametrize("N", [1, 2, 4, 8])
+@pytest.mark.parametrize("causal", [False, True])
+def test_ring_equals_full(N, causal):
+    rng = np.random.default_rng(10 + N)
+    S = 2 * N * 3
+    q, k, v = _rand(rng, S, 4, 2, 8)
+    O1, L1 = oracle.full_attention(q, k, v, causal)
+    O2, L2 = oracle.ring_attention(q, k, v, causal, N)
+    np.testing.assert_allclose(O2, O1, atol=1e-12)
+    np.testing.assert_allclose(L2, L1, atol=1e-12)
+
+
+def test_ring_rejects_unpadded_length():
+    q = np.zeros((10, 1, 2))
+    with pytest.raises(ValueError):
+        oracle.ring_attention(q, q, q, True, 4)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_ring_partials_merge_in_any_order(causal):
+    rng = np.random.default_rng(20)
+    N = 3
+    q, k, v = _rand(rng, 2 * N * 2, 2, 1, 4)
+    O_full, L_full = oracle.full_attention(q, k, v, causal)
+    parts, pos = oracle.ring_partials(q, k, v, causal, N)
+    for r in range(N):
+        for order in itertools.permutations(range(N)):
+            Op = np.stack([parts[r][s][0] for s in order])
+            Lp = np.stack([parts[r][s][1] for s in order])
+            O, L = oracle.lse_merge(Op, Lp)
+            np.testing.assert_allclose(O, O_full[pos[r]], atol=1e-12)
+            np.testing.assert_allclose(L, L_full[pos[r]], atol=1e-12)
+
+
+# ---------------------------------------------------------------- merge
+
+@pytest.mark.parametrize("case", load("merge_hand.json")["cases"], ids=lambda c: c["name"])
+def test_merge_hand_worked(case):
+    O, L = oracle.lse_merge(arr(case["o"]), arr(case["lse"]))
+    np.testing.assert_allclose(O, arr(case["O"]), atol=1e-12)
+    np.testing.assert_allclose(L, arr(case["LSE"]), atol=1e-12)
+
+
+def test_merge_single_partial_is_identity_and_order_free():
+    rng = np.random.default_rng(30)
+    o = rng.standard_normal((4, 3, 5, 6))
+    lse = rng.standard_normal((4, 3, 5))
+    O1, L1 = oracle.lse_merge(o[:1], lse[:1])
+    np.testing.assert_allclose(O1, o[0], atol=1e-15)
+    np.testing.assert_allclose(L1, lse[0], atol=1e-15)
+    O, L = oracle.lse_merge(o, lse)
+    for p in itertools.permutations(range(4)):
+        O2, L2 = oracle.lse_merge(o[list(p)], lse[list(p)])
+        np.testing.assert_allclose(O2, O, atol=1e-13)
+        np.testing.assert_allclose(L2, L, atol=1e-13)
+
+
+# ---------------------------------------------------------------- zigzag causal balance
+
+@pytest.mark.parametrize("N,c", [(1, 4), (2, 3), (4, 5), (8, 2), (16, 4)])
+def test_causal_pairs_equal_per_rank(N, c):
+    counts = oracle.causal_pairs_per_rank(N, c)
+    assert counts == [(2 * N - 1) * c * c + c * (c + 1)] * N
+
+
+def _visible_pairs_per_step(N, c, r, t):
+    s = (r - t) % N
+    qp = np.concatenate([np.arange(ch * c, ch * c + c) for ch in oracle.rank_chunks(N, r)])
+    kp = np.concatenate([np.arange(ch * c, ch * c + c) for ch in oracle.rank_chunks(N, s)])
+    return int((kp[None, :] <= qp[:, None]).sum())
+
+
+@pytest.mark.parametrize("N,c", [(2, 3), (4, 2), (8, 3)])
+def test_ring_step_liveness(N, c):
+    for r in range(N):
+        assert _visible_pairs_per_step(N, c, r, 0) == c * c + c * (c + 1)
+        for t in range(1, N):
+            assert _visible_pairs_per_step(N, c, r, t) == 2 * c * c
+
+
+@pytest.mark.parametrize("N,c,T", [(2, 8, 4), (4, 6, 2), (8, 4, 4), (3, 9, 3)])
+def test_causal_tiles_closed_form(N, c, T):
+    nt = c // T
+    full = (2 * N - 1) * nt * nt + nt * (nt - 1)
+    part = 2 * nt
+    skip = 2 * nt * 2 * N * nt - full - part
+    assert oracle.causal_tiles_per_rank(N, c, T) == [(full, part, skip)] * N
+
+
+def test_causal_tiles_ragged_totals():
+    N, c, T = 2, 5, 2          # tiles of 2,2,1 per chunk
+    res = oracle.causal_tiles_per_rank(N, c, T)
+    nt = 3
+    for full, part, skip in res:
+        assert full + part + skip == 2 * nt * 2 * N * nt
+    # every visible pair is covered by a full or partial tile exactly once
+    assert sum(oracle.causal_pairs_per_rank(N, c)) == (2 * N * c) * (2 * N * c + 1) // 2

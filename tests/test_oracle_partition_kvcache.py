@@ -1,0 +1,149 @@
+"""Pins of the zigzag partition, slot-mapping, scatter and decode oracles."""
+import numpy as np
+import pytest
+
+import oracle
+from oracle import kvcache as OK
+from tests._golden import load, arr
+
+pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
+
+
+# ---------------------------------------------------------------- zigzag
+
+@pytest.mark.parametrize("case", load("zigzag_hand.json")["cases"], ids=lambda c: c["name"])
+def test_zigzag_hand_worked(case):
+    perm, restore, padded = oracle.zigzag_partition(case["seq_lens"], case["n_ranks"])
+    assert perm.tolist() == case["perm"]
+    assert restore.tolist() == case["restore"]
+    assert padded.tolist() == case["padded_lens"]
+
+
+@pytest.mark.parametrize("N", [1, 2, 3, 8, 16])
+def test_zigzag_bijection_and_round_trip(N):
+    rng = np.random.default_rng(N)
+    lens = rng.integers(0, 200, size=5)
+    perm, restore, padded = oracle.zigzag_partition(lens, N)
+    total = int(lens.sum())
+    assert len(perm) == int(padded.sum())
+    assert np.all(padded % (2 * N) == 0) and np.all(padded >= lens) and np.all(padded - lens < 2 * N)
+    real = perm[perm >= 0]
+    assert sorted(real.tolist()) == list(range(total))          # bijection onto the tokens
+    assert np.array_equal(perm[restore], np.arange(total))      # perm o restore = id
+    x = rng.standard_normal((total, 3))
+    gathered = oracle.gather_rows(x, perm)
+    assert np.array_equal(gathered[perm < 0], np.zeros(((perm < 0).sum(), 3)))
+    assert np.array_equal(oracle.gather_rows(gathered, restore), x)
+
+
+def test_zigzag_rank_regions_hold_head_and_tail():
+    N, L = 4, 64
+    perm, _, _ = oracle.zigzag_partition([L], N)
+    c = L // (2 * N)
+    for r in range(N):
+        mine = perm[r * 2 * c:(r + 1) * 2 * c]
+        assert mine.tolist() == list(range(r * c, r * c + c)) + \
+            list(range((2 * N - 1 - r) * c, (2 * N - r) * c))
+
+
+# ---------------------------------------------------------------- slot mapping
+
+def test_slot_mapping_hand_worked_locations():
+    g = load("slot_mapping_hand.json")
+    for loc in g["locations"]:
+        assert OK.cp_token_location(loc["x"], g["block_size"], g["interleave"], g["pcp"], g["dcp"]) \
+            == (loc["vb"], loc["dev"], loc["off"])
+    ex = g["slot_example"]
+    slot = oracle.cp_slot_mapping(ex["query_start_loc"], ex["positions"], ex["block_table"],
+                                  g["block_size"], g["interleave"], g["pcp"], g["dcp"])
+    assert slot.tolist() == ex["slot"]
+
+
+def test_slot_mapping_rejects_bad_interleave():
+    for bad in load("slot_mapping_hand.json")["invalid"]:
+        with pytest.raises(ValueError):
+            oracle.cp_slot_mapping([0, 1], [0], [[0]], bad["block_size"], bad["interleave"],
+                                   bad["pcp"], bad["dcp"])
+
+
+@pytest.mark.parametrize("bs,I,pcp,dcp", [(128, 16, 2, 4), (16, 4, 1, 2), (8, 8, 3, 1), (12, 3, 2, 2)])
+def test_slot_mapping_is_a_balanced_bijection(bs, I, pcp, dcp):
+    W = pcp * dcp
+    V = bs * W
+    nvb = 3
+    x = np.arange(nvb * V)
+    bt = np.array([[7, 2, 11]])
+    slot = oracle.cp_slot_mapping([0, len(x)], x, bt, bs, I, pcp, dcp)
+    owners = (slot >= 0).sum(axis=0)
+    assert np.all(owners == 1)                                   # exactly one device per token
+    for w in range(W):
+        s = slot[w][slot[w] >= 0]
+        assert len(s) == nvb * bs                                # block_size tokens per full vblock
+        assert len(np.unique(s)) == len(s)                       # no two tokens share a slot
+        assert set((s // bs).tolist()) == {7, 2, 11}
+    # interleave: runs of I consecutive tokens stay on one device, then move to the next
+    dev = np.argmax(slot >= 0, axis=0)
+    assert np.array_equal(dev, (x % V) // I % W)
+
+
+# ---------------------------------------------------------------- decode
+
+def _tiny_decode_case(seed=0, R=3, ctx=(1, 37, 300), bs=8, I=2, pcp=2, dcp=2, Hq=4, Hkv=2, d=8):
+    rng = np.random.default_rng(seed)
+    W = pcp * dcp
+    V = bs * W
+    nvb = [-(-L // V) for L in ctx]
+    NB = sum(nvb) + 2
+    ids = rng.permutation(NB)
+    bt = np.full((R, max(nvb)), -1, dtype=np.int64)
+    p = 0
+    for r in range(R):
+        bt[r, :nvb[r]] = ids[p:p + nvb[r]]
+        p += nvb[r]
+    qsl = np.concatenate([[0], np.cumsum(ctx)])
+    pos = np.concatenate([np.arange(L) for L in ctx])
+    T = int(qsl[-1])
+    k = rng.standard_normal((T, Hkv, d))
+    v = rng.standard_normal((T, Hkv, d))
+    q = rng.standard_normal((R, Hq, d))
+    slot = oracle.cp_slot_mapping(qsl, pos, bt, bs, I, pcp, dcp)
+    kc = np.full((W, NB, Hkv, bs, d), np.nan)
+    vc = np.full((W, NB, Hkv, bs, d), np.nan)
+    oracle.cp_kv_scatter(k, v, slot, kc, vc, bs)
+    return dict(q=q, k=k, v=v, kc=kc, vc=vc, bt=bt, ctx=np.array(ctx), qsl=qsl, bs=bs, I=I,
+                pcp=pcp, dcp=dcp)
+
+
+@pytest.mark.parametrize("split_blocks", [1, 2, 5])
+def test_decode_equals_plain_attention_over_tokens(split_blocks):
+    c = _tiny_decode_case()
+    O, L = oracle.cp_decode(c["q"], c["kc"], c["vc"], c["bt"], c["ctx"], c["bs"], c["I"],
+                            c["pcp"], c["dcp"], split_blocks)
+    for r in range(len(c["ctx"])):
+        s0, s1 = c["qsl"][r], c["qsl"][r + 1]
+        Or, Lr = oracle.decode_reference(c["q"][r], c["k"][s0:s1], c["v"][s0:s1])
+        np.testing.assert_allclose(O[r], Or, atol=1e-12)
+        np.testing.assert_allclose(L[r], Lr, atol=1e-12)
+
+
+def test_decode_partials_cover_each_token_once():
+    c = _tiny_decode_case(seed=1, ctx=(300,), R=1)
+    Op, Lp, n_splits = oracle.cp_decode_partials(c["q"], c["kc"], c["vc"], c["bt"], c["ctx"],
+                                                 c["bs"], c["I"], c["pcp"], c["dcp"], 1)
+    # total weight across partials = total softmax mass over the request's keys
+    _, L_ref = oracle.decode_reference(c["q"][0], c["k"], c["v"])
+    mass = np.exp(Lp[:, 0, :])
+    np.testing.assert_allclose(np.log(mass.sum(axis=0)), L_ref, atol=1e-12)
+
+
+def test_planted_slot_formula_mistake_is_caught(monkeypatch):
+    # reading the cache with a wrong inverse (device and offset order swapped) must fail the pin
+    monkeypatch.setattr(OK, "_device_tokens",
+                        lambda w, vb, bs, I, W: vb * bs * W + (np.arange(bs) % I) * W + w)
+    c = _tiny_decode_case(seed=2)
+    O, _ = oracle.cp_decode(c["q"], c["kc"], c["vc"], c["bt"], c["ctx"], c["bs"], c["I"],
+                            c["pcp"], c["dcp"], 2)
+    r = 2
+    s0, s1 = c["qsl"][r], c["qsl"][r + 1]
+    Or, _ = oracle.decode_reference(c["q"][r], c["k"][s0:s1], c["v"][s0:s1])
+    assert not np.allclose(O[r], Or, atol=1e-6)
