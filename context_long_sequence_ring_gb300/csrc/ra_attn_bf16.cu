@@ -1,0 +1,570 @@
+// Ring-order attention forward, bf16 in / fp32 accumulate, on the 5th-gen
+// tensor cores (tcgen05.mma into tensor memory), fed by TMA.
+//
+// Method sources: "Parallelism-CP" diagram (Q/K/V split along the sequence;
+// K/V rotate around a ring of N ranks until every Q block has met every K/V
+// block); guijiagi.com "Ring Attention" tag page (ring step t: rank i uses the
+// K/V block of rank (i - t) mod N while the next block is in flight; the
+// blockwise decomposition softmax(QK^T)V = sum_j e^{s_j} V_j / sum_j e^{s_j}
+// with a running max and sum); vLLM-Ascend "Context Parallel (CP)" head-tail
+// partition (rank r owns chunks r and 2N-1-r); the causal mask is applied on
+// original positions.
+//
+// Single-GPU mapping of the ring:
+//  * the N ranks are virtual; a CTA owns one work item = one query head and a
+//    mirrored pair of 128-row query tiles of one rank (tile j of chunk r and
+//    tile nt-1-j of chunk 2N-1-r), so every item carries the same causal work
+//    (the zigzag balance, per tile instead of per rank);
+//  * for each query tile the K/V tiles are visited in ring order: ranks
+//    s = r, r-1, ..., r-N+1 (mod N), each rank's chunks s and 2N-1-s in turn;
+//    chunks that the causal mask hides are skipped, the diagonal tile is
+//    masked element-wise;
+//  * the ring's "receive the next block while computing this one" becomes a
+//    two-stage TMA ring of K and V tiles in shared memory guarded by mbarriers.
+//
+// Roles (192 threads): warp 0 issues TMA loads, warp 1 allocates tensor memory
+// and issues the MMAs (one thread), warps 2..5 run the online softmax (one
+// query row per thread, TMEM lane = row) and the epilogue.
+//
+// Tensor memory (512 columns): S0 = cols [0,128), S1 = [128,256) (double
+// buffered scores), O = [256, 256+D).  Shared memory (1024-aligned, 128-byte
+// swizzle, as TMA writes it): Q [128 x D], K[2] and V[2] [128 x D], P [128 x 128].
+//
+// Per K/V tile j the MMA thread issues S_j = Q K_j^T (D/16 MMAs of
+// 128x128x16), then O += P_{j-1} V_{j-1} (8 MMAs of 128xDx16) once the softmax
+// has published P_{j-1}; the softmax of tile j overlaps P_{j-1} V_{j-1} and
+// S_{j+1}.  O is rescaled in tensor memory only when a row's running max grows
+// by more than 2^8 (the stale max is exact as long as l and O use the same
+// reference and P stays in range).
+#include <cuda.h>
+#include <math_constants.h>
+
+#include <cstdlib>
+
+#include "ra_common.cuh"
+#include "ra_sm100.cuh"
+
+RA_DEFINE_ERROR_FETCH(fetch_error_attn_bf16)
+
+namespace {
+
+using namespace ra::sm100;
+
+constexpr int BM = 128;       // query rows per tile
+constexpr int BN = 128;       // keys per K/V tile
+constexpr int STAGES = 2;     // K/V shared-memory ring depth
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS0 = 0, kColO = 2 * BN;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// ------------------------------------------------------------------ schedule
+struct Sched {
+  int N, c, nt, causal;
+};
+
+// Iterates the K/V tiles one query tile (chunk qc, tile qi) meets, in ring
+// order.  kind: 0 = every pair visible, 1 = diagonal tile (mask j <= i).
+struct KvIter {
+  int N, nt, causal, qc, qi, r;
+  int t, h, ki;
+  __device__ void init(const Sched& s, int qc_, int qi_) {
+    N = s.N; nt = s.nt; causal = s.causal; qc = qc_; qi = qi_;
+    r = qc < N ? qc : 2 * N - 1 - qc;
+    t = 0; h = 0; ki = -1;
+  }
+  __device__ bool next(int& kc, int& kt) {
+    while (t < N) {
+      const int s = (r - t + N) % N;             // rank whose block is held at step t
+      const int ch = h == 0 ? s : 2 * N - 1 - s;  // its head, then its tail chunk
+      const int lim = !causal ? nt : (ch < qc ? nt : (ch == qc ? qi + 1 : 0));
+      ++ki;
+      if (ki < lim) { kc = ch; kt = ki; return true; }
+      ki = -1;
+      if (++h == 2) { h = 0; ++t; }
+    }
+    return false;
+  }
+};
+
+__device__ __forceinline__ int n_kv_tiles(const Sched& s, int qc, int qi) {
+  return s.causal ? qc * s.nt + qi + 1 : 2 * s.N * s.nt;
+}
+
+struct Params {
+  int B, Hq, Hkv, S, N, c, nt, causal, layout, group;
+  float scale_log2;
+  __nv_bfloat16* o;
+  float* lse;
+  long long wait_limit;
+};
+
+__device__ __forceinline__ int64_t token_row(const Params& p, int b, int ch, int off) {
+  if (p.layout == RA_LAYOUT_NATURAL) return static_cast<int64_t>(b) * p.S + static_cast<int64_t>(ch) * p.c + off;
+  const int rank = ch < p.N ? ch : 2 * p.N - 1 - ch;
+  const int half = ch < p.N ? 0 : 1;
+  return ((static_cast<int64_t>(rank) * p.B + b) * 2 + half) * p.c + off;
+}
+
+// Work item -> (b, hq, rank r, j).  The query heads that share one K/V head
+// are innermost so that concurrent CTAs stream the same K/V tiles (L2 reuse).
+struct Item {
+  int b, hq, g, r, j;
+};
+__device__ __forceinline__ Item decode_item(const Params& p, int idx) {
+  Item it;
+  const int hg = idx % p.group; idx /= p.group;
+  it.j = idx % p.nt; idx /= p.nt;
+  it.r = idx % p.N; idx /= p.N;
+  it.g = idx % p.Hkv; idx /= p.Hkv;
+  it.b = idx;
+  it.hq = it.g * p.group + hg;
+  return it;
+}
+// The two query tiles of an item: (chunk r, tile j) and (chunk 2N-1-r, tile nt-1-j).
+__device__ __forceinline__ void tile_of(const Params& p, const Item& it, int ti, int& qc, int& qi) {
+  if (ti == 0) { qc = it.r; qi = it.j; }
+  else { qc = 2 * p.N - 1 - it.r; qi = p.nt - 1 - it.j; }
+}
+
+template <int D>
+struct __align__(1024) Smem {
+  uint8_t q[BM * D * 2];
+  uint8_t k[STAGES][BN * D * 2];
+  uint8_t v[STAGES][BN * D * 2];
+  uint8_t p[BM * BN * 2];
+  uint64_t q_full, q_empty, k_full[STAGES], k_empty[STAGES], v_full[STAGES], v_empty[STAGES];
+  uint64_t s_full[2], s_empty[2], p_full, pv_done, o_empty, drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+__device__ __forceinline__ uint32_t f2_bf16x2(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    ring_attn_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                          const __grid_constant__ CUtensorMap tmV, const Params p) {
+  constexpr int SLABS = D / 64;                     // 64-column (128-byte) slabs of a Q/K/V tile
+  constexpr uint32_t kTileBytes = BM * D * 2;       // one Q, K or V tile
+  constexpr uint32_t kIdescS = idesc_bf16_f32(BM, BN, 0, 0);  // S = Q K^T, both K-major
+  constexpr uint32_t kIdescO = idesc_bf16_f32(BM, D, 0, 1);   // O += P V, V is MN-major
+
+  extern __shared__ uint8_t smem_raw[];
+  Smem<D>& sm = *reinterpret_cast<Smem<D>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const Item it = decode_item(p, blockIdx.x);
+  const Sched sch{p.N, p.c, p.nt, p.causal};
+  volatile int* abort_flag = &sm.abort_flag;
+  const long long lim = p.wait_limit;
+
+  // ---------------------------------------------------------------- set-up
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&sm.q_full), 1);
+    mbar_init(smem_u32(&sm.q_empty), 1);
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_u32(&sm.k_full[s]), 1);
+      mbar_init(smem_u32(&sm.k_empty[s]), 1);
+      mbar_init(smem_u32(&sm.v_full[s]), 1);
+      mbar_init(smem_u32(&sm.v_empty[s]), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_u32(&sm.s_full[s]), 1);
+      mbar_init(smem_u32(&sm.s_empty[s]), 128);
+    }
+    mbar_init(smem_u32(&sm.p_full), 128);
+    mbar_init(smem_u32(&sm.pv_done), 1);
+    mbar_init(smem_u32(&sm.o_empty), 128);
+    mbar_init(smem_u32(&sm.drain), 1);
+    sm.abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&sm.tmem_base), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+
+  if (warp == 0) {
+    // ============================================================ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      uint32_t kv_cnt = 0;
+      bool issued[STAGES] = {false, false};
+      uint32_t last_ph[STAGES] = {0, 0};
+      bool ok = true;
+      for (int ti = 0; ti < 2 && ok; ++ti) {
+        int qc, qi;
+        tile_of(p, it, ti, qc, qi);
+        if (!(ok = mbar_wait(smem_u32(&sm.q_empty), (ti & 1) ^ 1, abort_flag, lim, 1))) break;
+        const uint32_t qb = smem_u32(&sm.q_full);
+        mbar_arrive_expect_tx(qb, kTileBytes);
+        const int32_t qrow = static_cast<int32_t>(token_row(p, it.b, qc, qi * BM));
+        for (int s = 0; s < SLABS; ++s) tma_load_3d(smem_u32(sm.q + s * BM * 128), &tmQ, qb, 64 * s, it.hq, qrow);
+        KvIter kv;
+        kv.init(sch, qc, qi);
+        int kc, kt;
+        while (kv.next(kc, kt)) {
+          const int st = kv_cnt % STAGES;
+          const uint32_t ph = (kv_cnt / STAGES) & 1;
+          const int32_t krow = static_cast<int32_t>(token_row(p, it.b, kc, kt * BN));
+          if (!(ok = mbar_wait(smem_u32(&sm.k_empty[st]), ph ^ 1, abort_flag, lim, 2))) break;
+          mbar_arrive_expect_tx(smem_u32(&sm.k_full[st]), kTileBytes);
+          for (int s = 0; s < SLABS; ++s)
+            tma_load_3d(smem_u32(sm.k[st] + s * BN * 128), &tmK, smem_u32(&sm.k_full[st]), 64 * s, it.g, krow);
+          if (!(ok = mbar_wait(smem_u32(&sm.v_empty[st]), ph ^ 1, abort_flag, lim, 3))) break;
+          mbar_arrive_expect_tx(smem_u32(&sm.v_full[st]), kTileBytes);
+          for (int s = 0; s < SLABS; ++s)
+            tma_load_3d(smem_u32(sm.v[st] + s * BN * 128), &tmV, smem_u32(&sm.v_full[st]), 64 * s, it.g, krow);
+          issued[st] = true;
+          last_ph[st] = ph;
+          ++kv_cnt;
+        }
+      }
+      if (!ok) {
+        // let the copies already in flight land before the CTA exits
+        for (int s = 0; s < STAGES; ++s)
+          if (issued[s]) {
+            mbar_wait(smem_u32(&sm.k_full[s]), last_ph[s], abort_flag, 1 << 22, 0);
+            mbar_wait(smem_u32(&sm.v_full[s]), last_ph[s], abort_flag, 1 << 22, 0);
+          }
+      }
+    }
+  } else if (warp == 1) {
+    // ============================================================ MMA issuer
+    if (lane == 0) {
+      uint32_t kv_cnt = 0, s_cnt = 0, pv_cnt = 0;
+      bool ok = true;
+      const uint32_t q_base = smem_u32(sm.q), p_base = smem_u32(sm.p);
+      for (int ti = 0; ti < 2 && ok; ++ti) {
+        int qc, qi;
+        tile_of(p, it, ti, qc, qi);
+        const int nkv = n_kv_tiles(sch, qc, qi);
+        if (!(ok = mbar_wait(smem_u32(&sm.q_full), ti & 1, abort_flag, lim, 10))) break;
+        int prev_st = 0;
+        uint32_t prev_ph = 0;
+        // O += P_{jj} V_{jj}
+        auto do_pv = [&](int st, uint32_t ph, bool first) -> bool {
+          if (!mbar_wait(smem_u32(&sm.p_full), pv_cnt & 1, abort_flag, lim, 11)) return false;
+          if (!mbar_wait(smem_u32(&sm.v_full[st]), ph, abort_flag, lim, 12)) return false;
+          if (first && !mbar_wait(smem_u32(&sm.o_empty), (ti & 1) ^ 1, abort_flag, lim, 13)) return false;
+          tc_fence_after();
+          const uint32_t v_base = smem_u32(sm.v[st]);
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk) {
+            const uint64_t ad = desc_sw128(p_base + (kk >> 2) * (BM * 128) + (kk & 3) * 32, 16, 1024);
+            const uint64_t bd = desc_sw128(v_base + kk * 16 * 128, BN * 128, 1024);
+            mma_bf16_ss(tmem + kColO, ad, bd, kIdescO, (kk > 0 || !first) ? 1u : 0u);
+          }
+          mma_commit(smem_u32(&sm.pv_done));
+          mma_commit(smem_u32(&sm.v_empty[st]));
+          ++pv_cnt;
+          return true;
+        };
+        for (int j = 0; j < nkv && ok; ++j) {
+          const int st = kv_cnt % STAGES;
+          const uint32_t ph = (kv_cnt / STAGES) & 1;
+          const int sb = s_cnt & 1;
+          const uint32_t sph = (s_cnt >> 1) & 1;
+          if (!(ok = mbar_wait(smem_u32(&sm.k_full[st]), ph, abort_flag, lim, 14))) break;
+          if (!(ok = mbar_wait(smem_u32(&sm.s_empty[sb]), sph ^ 1, abort_flag, lim, 15))) break;
+          tc_fence_after();
+          const uint32_t k_base = smem_u32(sm.k[st]);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
+            const uint64_t ad = desc_sw128(q_base + off, 16, 1024);
+            const uint64_t bd = desc_sw128(k_base + (kk >> 2) * (BN * 128) + (kk & 3) * 32, 16, 1024);
+            mma_bf16_ss(tmem + kColS0 + sb * BN, ad, bd, kIdescS, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(smem_u32(&sm.s_full[sb]));
+          mma_commit(smem_u32(&sm.k_empty[st]));
+          if (j == nkv - 1) mma_commit(smem_u32(&sm.q_empty));
+          ++s_cnt;
+          if (j > 0 && !(ok = do_pv(prev_st, prev_ph, j - 1 == 0))) break;
+          prev_st = st;
+          prev_ph = ph;
+          ++kv_cnt;
+        }
+        if (ok) ok = do_pv(prev_st, prev_ph, nkv - 1 == 0);
+      }
+      // make sure no MMA is still writing tensor memory before it is freed
+      mma_commit(smem_u32(&sm.drain));
+      mbar_wait(smem_u32(&sm.drain), 0, abort_flag, ok ? lim : (1 << 22), 16);
+    }
+  } else {
+    // ============================================================ softmax + epilogue
+    const int quarter = warp & 3;                 // TMEM lane quarter this warp may access
+    const int row = quarter * 32 + lane;          // query row inside the tile
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const uint32_t p_base = smem_u32(sm.p);
+    uint32_t s_cnt = 0, pv_cnt = 0;
+    bool ok = true;
+    for (int ti = 0; ti < 2 && ok; ++ti) {
+      int qc, qi;
+      tile_of(p, it, ti, qc, qi);
+      const int q_valid = min(BM, p.c - qi * BM);
+      const int nkv = n_kv_tiles(sch, qc, qi);
+      KvIter kv;
+      kv.init(sch, qc, qi);
+      float m = -CUDART_INF_F, l = 0.f;
+      for (int j = 0; j < nkv; ++j) {
+        int kc = 0, kt = 0;
+        kv.next(kc, kt);
+        const int kv_valid = min(BN, p.c - kt * BN);
+        const bool diag = p.causal && kc == qc && kt == qi;
+        const int sb = s_cnt & 1;
+        const uint32_t sph = (s_cnt >> 1) & 1;
+        if (!(ok = mbar_wait(smem_u32(&sm.s_full[sb]), sph, abort_flag, lim, 20))) break;
+        tc_fence_after();
+        uint32_t sr[BN];
+#pragma unroll
+        for (int c4 = 0; c4 < BN / 32; ++c4)
+          tmem_ld32(t_lane + kColS0 + sb * BN + 32 * c4, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * c4]));
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(smem_u32(&sm.s_empty[sb]));
+        ++s_cnt;
+        // mask (raw scores) and row max
+        const int col_lim = diag ? min(kv_valid, row + 1) : kv_valid;
+        float mx = -CUDART_INF_F;
+#pragma unroll
+        for (int i = 0; i < BN; ++i) {
+          float x = __uint_as_float(sr[i]);
+          if (i >= col_lim) x = -CUDART_INF_F;
+          sr[i] = __float_as_uint(x);
+          mx = fmaxf(mx, x);
+        }
+        const float m_tile = mx * p.scale_log2;
+        const bool need = (j == 0) || (m_tile > m + 8.f);
+        const float m_use = need ? fmaxf(m, m_tile) : m;
+        const float m_ref = (m_use == -CUDART_INF_F) ? 0.f : m_use;
+        const float alpha = (j == 0) ? 0.f : exp2f(m - m_ref);
+        float rs = 0.f;
+#pragma unroll
+        for (int i = 0; i < BN; i += 2) {
+          const float p0 = exp2f(fmaf(__uint_as_float(sr[i]), p.scale_log2, -m_ref));
+          const float p1 = exp2f(fmaf(__uint_as_float(sr[i + 1]), p.scale_log2, -m_ref));
+          rs += p0 + p1;
+          sr[i >> 1] = f2_bf16x2(p0, p1);   // packed P in the first BN/2 words
+        }
+        l = (j == 0) ? rs : l * alpha + rs;
+        if (j > 0) {
+          // P_{j-1} V_{j-1} must be complete: P buffer reuse and O rescale
+          if (!(ok = mbar_wait(smem_u32(&sm.pv_done), pv_cnt & 1, abort_flag, lim, 21))) break;
+          ++pv_cnt;
+          tc_fence_after();
+          if (__any_sync(0xffffffffu, need && alpha != 1.f)) {
+            const float a = need ? alpha : 1.f;
+#pragma unroll
+            for (int c4 = 0; c4 < D / 32; ++c4) {
+              uint32_t orr[32];
+              tmem_ld32(t_lane + kColO + 32 * c4, orr);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * a);
+              tmem_st32(t_lane + kColO + 32 * c4, orr);
+            }
+            tmem_wait_st();
+          }
+        }
+        m = m_use;
+        // P (bf16, 128-byte swizzle, K-major) into shared memory
+#pragma unroll
+        for (int ch = 0; ch < BN / 8; ++ch) {
+          const int slab = ch >> 3, c16 = ch & 7;
+          const uint32_t addr = p_base + slab * (BM * 128) + row * 128 + ((c16 ^ (row & 7)) << 4);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(sr[4 * ch]),
+                       "r"(sr[4 * ch + 1]), "r"(sr[4 * ch + 2]), "r"(sr[4 * ch + 3])
+                       : "memory");
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(smem_u32(&sm.p_full));
+      }
+      if (!ok) break;
+      // ---------------------------------------------------------- epilogue
+      if (!(ok = mbar_wait(smem_u32(&sm.pv_done), pv_cnt & 1, abort_flag, lim, 22))) break;
+      ++pv_cnt;
+      tc_fence_after();
+      const float inv_l = l > 0.f ? 1.f / l : 0.f;
+      const bool row_ok = row < q_valid;
+      const int64_t trow = token_row(p, it.b, qc, qi * BM + row);
+      __nv_bfloat16* orow = p.o + (trow * p.Hq + it.hq) * D;
+#pragma unroll
+      for (int c4 = 0; c4 < D / 32; ++c4) {
+        uint32_t orr[32];
+        tmem_ld32(t_lane + kColO + 32 * c4, orr);
+        tmem_wait_ld();
+        if (row_ok) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 8) {
+            uint4 pk;
+            pk.x = f2_bf16x2(__uint_as_float(orr[i]) * inv_l, __uint_as_float(orr[i + 1]) * inv_l);
+            pk.y = f2_bf16x2(__uint_as_float(orr[i + 2]) * inv_l, __uint_as_float(orr[i + 3]) * inv_l);
+            pk.z = f2_bf16x2(__uint_as_float(orr[i + 4]) * inv_l, __uint_as_float(orr[i + 5]) * inv_l);
+            pk.w = f2_bf16x2(__uint_as_float(orr[i + 6]) * inv_l, __uint_as_float(orr[i + 7]) * inv_l);
+            *reinterpret_cast<uint4*>(orow + 32 * c4 + i) = pk;
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(smem_u32(&sm.o_empty));
+      if (row_ok) p.lse[trow * p.Hq + it.hq] = l > 0.f ? (m + log2f(l)) * kLn2 : -CUDART_INF_F;
+    }
+  }
+
+  // ---------------------------------------------------------------- teardown
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+// Per-rank tile classification with the kernel's own iterator (for tests).
+__global__ void schedule_counts_kernel(Sched s, unsigned long long* counts) {
+  const int n_tiles = 2 * s.N * s.nt;  // query tiles of the whole sequence
+  for (int idx = blockIdx.x * blockDim.x + threadIdx.x; idx < n_tiles; idx += gridDim.x * blockDim.x) {
+    const int qc = idx / s.nt, qi = idx % s.nt;
+    const int r = qc < s.N ? qc : 2 * s.N - 1 - qc;
+    KvIter kv;
+    kv.init(s, qc, qi);
+    int kc, kt;
+    unsigned long long full = 0, diag = 0, seen = 0;
+    while (kv.next(kc, kt)) {
+      ++seen;
+      const int qv = min(BM, s.c - qi * BM), kvv = min(BN, s.c - kt * BN);
+      const bool d = s.causal && kc == qc && kt == qi && !(qv == 1 && kvv == 1);
+      if (d) ++diag; else ++full;
+    }
+    if (static_cast<int>(seen) != n_kv_tiles(s, qc, qi)) ra_record_error(RA_ERR_DEVICE_BOUNDS, 30);
+    atomicAdd(&counts[r * 3 + 0], full);
+    atomicAdd(&counts[r * 3 + 1], diag);
+    atomicAdd(&counts[r * 3 + 2], static_cast<unsigned long long>(2 * s.N * s.nt) - seen);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+using EncodeTiledFn = decltype(&cuTensorMapEncodeTiled);
+
+EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+
+// Token-major [rows, H, D] bf16 tensor; box = 64 columns x 1 head x 128 rows,
+// 128-byte swizzle (the layout the MMA descriptors expect).
+ra_status make_map(CUtensorMap* map, const void* base, int D, int H, int64_t rows) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return ra::fail(RA_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(H) * D * 2};
+  cuuint32_t box[3] = {64, 1, 128};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return ra::fail(RA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+  return RA_OK;
+}
+
+template <int D>
+ra_status launch_bf16(const void* q, const void* k, const void* v, const Params& prm, int64_t items,
+                      cudaStream_t stream) {
+  CUtensorMap mq, mk, mv;
+  const int64_t rows = static_cast<int64_t>(prm.B) * prm.S;
+  ra_status st;
+  if ((st = make_map(&mq, q, D, prm.Hq, rows)) != RA_OK) return st;
+  if ((st = make_map(&mk, k, D, prm.Hkv, rows)) != RA_OK) return st;
+  if ((st = make_map(&mv, v, D, prm.Hkv, rows)) != RA_OK) return st;
+  const size_t smem = sizeof(Smem<D>) + 1024;
+  RA_CUDA_TRY(cudaFuncSetAttribute(ring_attn_bf16_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   static_cast<int>(smem)));
+  ring_attn_bf16_kernel<D><<<static_cast<unsigned>(items), kThreads, smem, stream>>>(mq, mk, mv, prm);
+  RA_LAUNCH_CHECK("ring_attn_bf16_kernel");
+  return RA_OK;
+}
+
+}  // namespace
+
+namespace ra {
+ra_status ring_attn_fwd_f32(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                            int Hkv, int S, int d, int causal, int N, float scale, int layout,
+                            cudaStream_t stream);
+
+// Bound of every device-side wait, in SM clock cycles: ~0.5 s by default,
+// overridable with the environment variable RA_WAIT_LIMIT_CYCLES.
+static long long wait_limit() {
+  static long long lim = [] {
+    const char* e = getenv("RA_WAIT_LIMIT_CYCLES");
+    long long v = e ? atoll(e) : 0;
+    return v > 0 ? v : (1ll << 30);
+  }();
+  return lim;
+}
+}  // namespace ra
+
+extern "C" ra_status ra_ring_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int32_t B,
+                                      int32_t Hq, int32_t Hkv, int32_t S, int32_t d, ra_dtype dt, int32_t causal,
+                                      int32_t n_ranks, float scale, ra_layout layout, ra_stream stream) {
+  ra::clear_error();
+  RA_REQUIRE(B >= 1 && Hq >= 1 && Hkv >= 1 && S >= 1, "B, Hq, Hkv, S must be >= 1");
+  RA_REQUIRE(Hq % Hkv == 0, "Hq (%d) must be a multiple of Hkv (%d)", Hq, Hkv);
+  RA_REQUIRE(n_ranks >= 1, "n_ranks must be >= 1 (got %d)", n_ranks);
+  RA_REQUIRE(S % (2 * n_ranks) == 0, "S (%d) must be a multiple of 2*n_ranks (%d); pad with ra_zigzag_partition",
+             S, 2 * n_ranks);
+  RA_REQUIRE(static_cast<int64_t>(B) * S < (int64_t(1) << 31), "B*S must be < 2^31");
+  RA_REQUIRE(dt == RA_F32 || dt == RA_BF16, "unknown dtype");
+  RA_REQUIRE(layout == RA_LAYOUT_NATURAL || layout == RA_LAYOUT_ZIGZAG, "unknown layout");
+  if (d != 64 && d != 128) return ra::fail(RA_ERR_UNSUPPORTED, "head dim %d not supported (64 or 128)", d);
+  RA_REQUIRE(q && k && v && o && lse, "NULL pointer");
+  RA_REQUIRE(ra::aligned16(q) && ra::aligned16(k) && ra::aligned16(v) && ra::aligned16(o) &&
+                 reinterpret_cast<uintptr_t>(lse) % 4 == 0,
+             "q, k, v, o must be 16-byte aligned");
+  const float sc = scale > 0.f ? scale : 1.f / sqrtf(static_cast<float>(d));
+  if (dt == RA_F32) return ra::ring_attn_fwd_f32(q, k, v, o, lse, B, Hq, Hkv, S, d, causal ? 1 : 0, n_ranks, sc,
+                                                 layout, stream);
+  Params prm;
+  prm.B = B; prm.Hq = Hq; prm.Hkv = Hkv; prm.S = S; prm.N = n_ranks; prm.c = S / (2 * n_ranks);
+  prm.nt = static_cast<int>(ra::ceil_div(prm.c, BM));
+  prm.causal = causal ? 1 : 0; prm.layout = layout; prm.group = Hq / Hkv;
+  prm.scale_log2 = sc * 1.4426950408889634f;
+  prm.o = static_cast<__nv_bfloat16*>(o); prm.lse = lse;
+  prm.wait_limit = ra::wait_limit();
+  const int64_t items = static_cast<int64_t>(B) * Hkv * n_ranks * prm.nt * prm.group;
+  RA_REQUIRE(items < (int64_t(1) << 31), "too many work items");
+  if (d == 128) return launch_bf16<128>(q, k, v, prm, items, stream);
+  return launch_bf16<64>(q, k, v, prm, items, stream);
+}
+
+extern "C" ra_status ra_ring_schedule_counts(int32_t S, int32_t n_ranks, int32_t causal, int64_t* counts,
+                                             ra_stream stream) {
+  ra::clear_error();
+  RA_REQUIRE(n_ranks >= 1 && S >= 1 && S % (2 * n_ranks) == 0, "S must be a positive multiple of 2*n_ranks");
+  RA_REQUIRE(counts != nullptr && reinterpret_cast<uintptr_t>(counts) % 8 == 0, "counts must be 8-byte aligned");
+  Sched s{n_ranks, S / (2 * n_ranks), static_cast<int>(ra::ceil_div(S / (2 * n_ranks), BM)), causal ? 1 : 0};
+  RA_CUDA_TRY(cudaMemsetAsync(counts, 0, sizeof(int64_t) * 3 * n_ranks, stream));
+  const int n_tiles = 2 * s.N * s.nt;
+  schedule_counts_kernel<<<static_cast<unsigned>(ra::ceil_div(n_tiles, 128)), 128, 0, stream>>>(
+      s, reinterpret_cast<unsigned long long*>(counts));
+  RA_LAUNCH_CHECK("schedule_counts_kernel");
+  return RA_OK;
+}

@@ -1,0 +1,254 @@
+"""Thin Python binding of libringattn.so (argument marshalling only).
+
+Every computation runs in the library's CUDA kernels; this module checks
+shapes/dtypes, passes raw device pointers and the current CUDA stream, and
+turns a non-zero ``ra_status`` into ``RingAttnError``.  There is no fallback:
+if the library is not built, or no GPU is present, calls fail loudly.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import torch
+
+from .build import LIB
+
+RA_OK, RA_ERR_INVALID_ARG, RA_ERR_UNSUPPORTED, RA_ERR_CUDA, RA_ERR_TIMEOUT, RA_ERR_DEVICE_BOUNDS = range(6)
+RA_F32, RA_BF16 = 0, 1
+LAYOUTS = {"natural": 0, "zigzag": 1}
+
+_c = ctypes
+_vp, _i32, _i64, _u64, _f32, _sz = _c.c_void_p, _c.c_int32, _c.c_int64, _c.c_uint64, _c.c_float, _c.c_size_t
+
+# name -> argument types (restype is ra_status unless noted)
+SIGNATURES = {
+    "ra_device_status": [_vp],
+    "ra_zigzag_partition": [_c.POINTER(_i64), _i32, _i32, _vp, _vp, _c.POINTER(_i64), _c.POINTER(_i64), _vp],
+    "ra_gather_rows": [_vp, _i64, _vp, _vp, _i64, _i64, _vp],
+    "ra_ring_attn_fwd": [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _c.c_int, _i32, _i32, _f32,
+                         _c.c_int, _vp],
+    "ra_ring_schedule_counts": [_i32, _i32, _i32, _vp, _vp],
+    "ra_lse_merge": [_vp, _vp, _i32, _i64, _i32, _i32, _vp, _c.c_int, _vp, _vp],
+    "ra_cp_slot_mapping": [_vp, _vp, _vp, _i32, _i32, _i64, _i32, _i32, _i32, _i32, _vp, _vp],
+    "ra_cp_kv_scatter": [_vp, _vp, _vp, _vp, _vp, _i64, _i32, _i32, _i32, _i32, _i64, _c.c_int, _vp],
+    "ra_cp_decode_workspace_size": [_i32, _i32, _i32, _i32, _i32, _i32, _i32, _c.POINTER(_sz)],
+    "ra_cp_decode": [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i64, _f32,
+                     _i32, _vp, _c.c_int, _vp, _vp, _sz, _vp],
+    "ra_selftest_wait_timeout": [_i64, _vp],
+    "ra_synth_fill": [_u64, _i64, _vp, _i32, _vp, _vp],
+}
+STRING_FUNCS = ["ra_last_error", "ra_version"]
+
+
+class RingAttnError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__("ra_status %d: %s" % (status, msg))
+        self.status = status
+
+
+_lib = None
+
+
+def lib():
+    """The loaded library (ctypes), with argument types set."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB):
+            raise RuntimeError("libringattn.so is not built: run __graft_entry__.build() "
+                               "(python -m context_long_sequence_ring_gb300.build)")
+        L = ctypes.CDLL(LIB)
+        for name, args in SIGNATURES.items():
+            f = getattr(L, name)
+            f.argtypes = args
+            f.restype = _c.c_int
+        for name in STRING_FUNCS:
+            getattr(L, name).restype = _c.c_char_p
+            getattr(L, name).argtypes = []
+        _lib = L
+    return _lib
+
+
+def last_error() -> str:
+    return lib().ra_last_error().decode()
+
+
+def version() -> str:
+    return lib().ra_version().decode()
+
+
+def _check(status: int):
+    if status != RA_OK:
+        raise RingAttnError(status, last_error())
+
+
+def _stream() -> int:
+    return torch.cuda.current_stream().cuda_stream
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError("tensor must be on a CUDA device")
+        if t is not None and not t.is_contiguous():
+            raise ValueError("tensor must be contiguous")
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return RA_BF16
+    if t.dtype == torch.float32:
+        return RA_F32
+    raise ValueError("dtype must be bfloat16 or float32")
+
+
+def device_status() -> int:
+    """Synchronise the current stream and return (and clear) the device error status."""
+    return lib().ra_device_status(_stream())
+
+
+# ---------------------------------------------------------------------- partition
+
+def zigzag_partition(seq_lens: Sequence[int], n_ranks: int, device="cuda"):
+    """(perm int32 [G], restore int32 [sum L]) of the head-tail partition."""
+    n = len(seq_lens)
+    arr = (_i64 * max(n, 1))(*[int(x) for x in seq_lens])
+    G, T = _i64(0), _i64(0)
+    _check(lib().ra_zigzag_partition(arr, n, n_ranks, None, None, _c.byref(G), _c.byref(T), _stream()))
+    perm = torch.empty(G.value, dtype=torch.int32, device=device)
+    restore = torch.empty(T.value, dtype=torch.int32, device=device)
+    if G.value > 0:
+        _check(lib().ra_zigzag_partition(arr, n, n_ranks, _ptr(perm), _ptr(restore), None, None, _stream()))
+    return perm, restore
+
+
+def gather_rows(src: torch.Tensor, idx: torch.Tensor, out: Optional[torch.Tensor] = None):
+    """out[i] = src[idx[i]] (zero rows where idx < 0); rows are the first dim."""
+    _need_cuda(src, idx, out)
+    if idx.dtype != torch.int32:
+        raise ValueError("idx must be int32")
+    rows = idx.numel()
+    if out is None:
+        out = torch.empty((rows,) + tuple(src.shape[1:]), dtype=src.dtype, device=src.device)
+    row_bytes = src[0].numel() * src.element_size() if src.shape[0] > 0 else 0
+    _check(lib().ra_gather_rows(_ptr(src), src.shape[0], _ptr(idx), _ptr(out), rows, row_bytes, _stream()))
+    return out
+
+
+# ---------------------------------------------------------------------- attention
+
+def ring_attn_fwd(q, k, v, causal: bool, n_ranks: int, B: int = 1, scale: Optional[float] = None,
+                  layout: str = "natural", o=None, lse=None):
+    """Ring-order attention forward.  q [B*S, Hq, d], k/v [B*S, Hkv, d] token-major.
+
+    Returns (O [B*S, Hq, d] in q's dtype, LSE float32 [B*S, Hq])."""
+    _need_cuda(q, k, v, o, lse)
+    rows, Hq, d = q.shape
+    Hkv = k.shape[1]
+    if rows % B != 0:
+        raise ValueError("rows of q must be a multiple of B")
+    S = rows // B
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((rows, Hq), dtype=torch.float32, device=q.device)
+    _check(lib().ra_ring_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, S, d, _dt(q),
+                                  1 if causal else 0, n_ranks, float(scale or 0.0), LAYOUTS[layout], _stream()))
+    return o, lse
+
+
+def ring_schedule_counts(S: int, n_ranks: int, causal: bool, device="cuda"):
+    out = torch.empty((n_ranks, 3), dtype=torch.int64, device=device)
+    _check(lib().ra_ring_schedule_counts(S, n_ranks, 1 if causal else 0, _ptr(out), _stream()))
+    return out
+
+
+def lse_merge(o_parts, lse_parts, out_dtype=torch.float32):
+    """Merge partials o_parts [P, T, H, d] fp32 with lse_parts [P, T, H] -> (O [T, H, d], LSE [T, H])."""
+    _need_cuda(o_parts, lse_parts)
+    P, T, H, d = o_parts.shape
+    o = torch.empty((T, H, d), dtype=out_dtype, device=o_parts.device)
+    lse = torch.empty((T, H), dtype=torch.float32, device=o_parts.device)
+    _check(lib().ra_lse_merge(_ptr(o_parts), _ptr(lse_parts), P, T, H, d, _ptr(o),
+                              RA_BF16 if out_dtype == torch.bfloat16 else RA_F32, _ptr(lse), _stream()))
+    return o, lse
+
+
+# ---------------------------------------------------------------------- KV cache
+
+def cp_slot_mapping(query_start_loc, positions, block_table, block_size: int, interleave: int, pcp: int,
+                    dcp: int, out=None):
+    _need_cuda(query_start_loc, positions, block_table, out)
+    R = query_start_loc.numel() - 1
+    T = positions.numel()
+    W = pcp * dcp
+    if out is None:
+        out = torch.empty((W, T), dtype=torch.int32, device=positions.device)
+    _check(lib().ra_cp_slot_mapping(_ptr(query_start_loc), _ptr(positions), _ptr(block_table),
+                                    block_table.shape[1], R, T, block_size, interleave, pcp, dcp, _ptr(out),
+                                    _stream()))
+    return out
+
+
+def cp_kv_scatter(k, v, slot, k_cache, v_cache):
+    _need_cuda(k, v, slot, k_cache, v_cache)
+    W, NB, Hkv, bs, d = k_cache.shape
+    _check(lib().ra_cp_kv_scatter(_ptr(k), _ptr(v), _ptr(slot), _ptr(k_cache), _ptr(v_cache), k.shape[0], W, Hkv,
+                                  d, bs, NB, _dt(k), _stream()))
+
+
+def cp_decode_workspace_size(R, Hq, d, max_vblocks, pcp, dcp, split_blocks) -> int:
+    n = _sz(0)
+    _check(lib().ra_cp_decode_workspace_size(R, Hq, d, max_vblocks, pcp, dcp, split_blocks, _c.byref(n)))
+    return n.value
+
+
+def cp_decode(q, k_cache, v_cache, block_table, ctx_lens, interleave: int, pcp: int, dcp: int,
+              split_blocks: int = 8, scale: Optional[float] = None, out_dtype=torch.bfloat16,
+              workspace=None, o=None, lse=None):
+    """Decode of one query token per request over the sharded cache -> (O [R, Hq, d], LSE [R, Hq])."""
+    _need_cuda(q, k_cache, v_cache, block_table, ctx_lens, workspace, o, lse)
+    R, Hq, d = q.shape
+    W, NB, Hkv, bs, _ = k_cache.shape
+    if W != pcp * dcp:
+        raise ValueError("cache has %d devices, pcp*dcp = %d" % (W, pcp * dcp))
+    max_vb = block_table.shape[1]
+    need = cp_decode_workspace_size(R, Hq, d, max_vb, pcp, dcp, split_blocks)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    if o is None:
+        o = torch.empty((R, Hq, d), dtype=out_dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty((R, Hq), dtype=torch.float32, device=q.device)
+    _check(lib().ra_cp_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(ctx_lens), R, Hq, Hkv,
+                              d, bs, interleave, pcp, dcp, max_vb, NB, float(scale or 0.0), split_blocks, _ptr(o),
+                              RA_BF16 if o.dtype == torch.bfloat16 else RA_F32, _ptr(lse), _ptr(workspace),
+                              workspace.numel() * workspace.element_size(), _stream()))
+    return o, lse
+
+
+# ---------------------------------------------------------------------- misc
+
+def selftest_wait_timeout(limit_cycles: int):
+    _check(lib().ra_selftest_wait_timeout(int(limit_cycles), _stream()))
+
+
+_TABLES = {}
+
+
+def synth_fill(key: int, table_cpu: torch.Tensor, shape, device="cuda"):
+    """Device tensor of the counter-based draw (see inputs.py) with the given key and value table."""
+    dev = torch.device(device)
+    tk = (table_cpu.dtype, dev)
+    if tk not in _TABLES:
+        _TABLES[tk] = table_cpu.to(dev)
+    table = _TABLES[tk]
+    out = torch.empty(tuple(shape), dtype=table_cpu.dtype, device=dev)
+    _check(lib().ra_synth_fill(_u64(key), out.numel(), _ptr(table), table.element_size(), _ptr(out), _stream()))
+    return out

@@ -1,0 +1,243 @@
+/*
+ * ringattn.h -- C ABI of libringattn.so: ring-order (context-parallel)
+ * attention, its zigzag token partition, the LSE merge and the
+ * context-parallel KV-cache decode path, on one GB300 (sm_103a).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Every function returns ra_status; nothing is thrown across the ABI.
+ *   On failure ra_last_error() (thread-local) describes the first problem.
+ * - Arguments are validated on the host before anything is launched: an
+ *   invalid argument launches nothing.
+ * - The caller owns every buffer.  The library never allocates device
+ *   memory; where scratch is needed the caller passes a workspace whose size
+ *   a *_workspace_size function reports.
+ * - "device" pointers are CUDA global-memory addresses of the current device;
+ *   "host" pointers are ordinary CPU memory read during the call.
+ * - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *   stream) and is asynchronous: outputs are ready once the stream is.
+ * - Kernels never trap.  A bounded device-side wait that expires, or a
+ *   device-side bounds check that fails, records a status in a device error
+ *   word; ra_device_status() synchronises the stream and returns (and clears)
+ *   it.
+ * - Tensors are dense and row-major in the layouts stated per function.
+ *   Token-major layouts put all heads of a token together: [tokens, H, d].
+ */
+#ifndef RINGATTN_H
+#define RINGATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* ra_stream; /* == cudaStream_t */
+
+typedef enum ra_status {
+  RA_OK = 0,
+  RA_ERR_INVALID_ARG = 1, /* bad size, pointer, alignment or rule violation */
+  RA_ERR_UNSUPPORTED = 2, /* valid, but not implemented (e.g. head dim)     */
+  RA_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed              */
+  RA_ERR_TIMEOUT = 4,     /* a bounded device wait expired                  */
+  RA_ERR_DEVICE_BOUNDS = 5 /* a device-side index check failed (input data) */
+} ra_status;
+
+typedef enum ra_dtype { RA_F32 = 0, RA_BF16 = 1 } ra_dtype;
+
+/* Token order of the attention tensors.
+ * RA_LAYOUT_NATURAL: row of (sequence b, position p) = b*S + p.
+ * RA_LAYOUT_ZIGZAG : the gathered head-tail order of ra_zigzag_partition for
+ *   B sequences of equal length S: rank-major, then sequence, then the rank's
+ *   two chunks (chunk r, then chunk 2N-1-r), each S/(2N) tokens long; the row
+ *   of (rank r, sequence b, half h, offset o) is ((r*B + b)*2 + h)*S/(2N) + o.
+ *   This is what N context-parallel ranks hold, concatenated. */
+typedef enum ra_layout { RA_LAYOUT_NATURAL = 0, RA_LAYOUT_ZIGZAG = 1 } ra_layout;
+
+/* Thread-local description of the last failure ("" if none). */
+const char* ra_last_error(void);
+
+/* Library version string. */
+const char* ra_version(void);
+
+/* Synchronise `stream`, then return and clear the device error word of every
+ * kernel module (RA_OK if no kernel recorded a problem).  A CUDA error seen
+ * while synchronising is returned as RA_ERR_CUDA. */
+ra_status ra_device_status(ra_stream stream);
+
+/* ------------------------------------------------------------------------
+ * ra_zigzag_partition -- head-tail token partition and its restore index.
+ * Source: vLLM-Ascend developer guide "Context Parallel (CP)", section
+ * "Prefill context parallel (PCP)", head-tail token partition (pad, cut into
+ * 2*pcp equal parts, pair part i with part 2*pcp-1-i, pcp_allgather_restore_idx).
+ *
+ * seq_lens   host   int64 [num_seqs], lengths L_q >= 0 (tokens packed request
+ *                   after request, unpadded, in the original order).
+ * n_ranks    N >= 1 context-parallel ranks.
+ * perm       device int32 [G] out, G = sum_q ceil(L_q/2N)*2N: perm[g] is the
+ *                   original token index at gathered position g, -1 for a pad
+ *                   position.  Gathered order: rank-major, then request, then
+ *                   (chunk r, chunk 2N-1-r) of that request.
+ * restore    device int32 [sum L_q] out: restore[i] = gathered position of
+ *                   original token i (restore = perm^-1).
+ * padded_total, total  host int64 out (may be NULL): G and sum L_q.
+ * Either of perm/restore may be NULL to query the sizes only (then nothing is
+ * launched).  Errors: num_seqs < 0, n_ranks < 1, negative length, G >= 2^31.
+ * ---------------------------------------------------------------------- */
+ra_status ra_zigzag_partition(const int64_t* seq_lens, int32_t num_seqs, int32_t n_ranks,
+                              int32_t* perm, int32_t* restore, int64_t* padded_total,
+                              int64_t* total, ra_stream stream);
+
+/* ------------------------------------------------------------------------
+ * ra_gather_rows -- dst[i, :] = src[idx[i], :] (a zero row where idx[i] < 0).
+ * The data movement of the zigzag permute (idx = perm) and of the restore
+ * (idx = restore), same source as ra_zigzag_partition.
+ *
+ * src  device [src_rows, row_bytes] bytes; idx device int32 [rows];
+ * dst  device [rows, row_bytes] out (must not overlap src).
+ * An idx >= src_rows is a device-side bounds error (row zero-filled,
+ * RA_ERR_DEVICE_BOUNDS recorded).
+ * ---------------------------------------------------------------------- */
+ra_status ra_gather_rows(const void* src, int64_t src_rows, const int32_t* idx, void* dst,
+                         int64_t rows, int64_t row_bytes, ra_stream stream);
+
+/* ------------------------------------------------------------------------
+ * ra_ring_attn_fwd -- causal or full GQA attention forward computed in ring
+ * order over N virtual context-parallel ranks with blockwise online softmax.
+ * Sources: "Parallelism-CP" diagram (Q/K/V split along the sequence, K/V
+ * rotate on a ring, every Q block meets every K/V block); guijiagi.com
+ * "Ring Attention" tag page (ring step t: rank i uses the K/V of rank
+ * (i - t) mod N; blockwise decomposition with running max and running sum);
+ * vLLM-Ascend "Context Parallel (CP)" head-tail partition (rank r owns chunks
+ * r and 2N-1-r).  The result equals full softmax attention.
+ *
+ * q    device [B*S, Hq, d]  (dtype dt), token order per `layout`.
+ * k, v device [B*S, Hkv, d] (dtype dt), same token order.
+ * o    device [B*S, Hq, d]  out, dtype dt, same token order.
+ * lse  device float [B*S, Hq] out: natural-log sum of exp(scaled scores).
+ * Query head h reads K/V head h / (Hq/Hkv).  scale <= 0 means 1/sqrt(d).
+ * causal != 0: the query at original position i sees keys j <= i.
+ * Requirements: B, Hq, Hkv, S >= 1; Hq % Hkv == 0; S % (2*n_ranks) == 0;
+ * B*S < 2^31; pointers 16-byte aligned.  d must be 64 or 128
+ * (RA_ERR_UNSUPPORTED otherwise).  RA_BF16 runs on the tensor cores
+ * (tcgen05, fp32 accumulation); RA_F32 runs an exact fp32 SIMT kernel.
+ * ---------------------------------------------------------------------- */
+ra_status ra_ring_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                           int32_t B, int32_t Hq, int32_t Hkv, int32_t S, int32_t d,
+                           ra_dtype dt, int32_t causal, int32_t n_ranks, float scale,
+                           ra_layout layout, ra_stream stream);
+
+/* ------------------------------------------------------------------------
+ * ra_ring_schedule_counts -- the (query tile, key tile) classification the
+ * bf16 ring kernel uses, counted per virtual rank on the device by the same
+ * schedule code: counts[r*3 + {0,1,2}] = tile pairs processed without mask,
+ * with the causal diagonal mask, and skipped.  Tiles are 128 tokens, cut per
+ * chunk (the last tile of a chunk may be shorter).
+ * counts  device int64 [n_ranks*3] out.  Same size rules as ra_ring_attn_fwd.
+ * ---------------------------------------------------------------------- */
+ra_status ra_ring_schedule_counts(int32_t S, int32_t n_ranks, int32_t causal, int64_t* counts,
+                                  ra_stream stream);
+
+/* ------------------------------------------------------------------------
+ * ra_lse_merge -- merge P partial attention results (the update of a
+ * cp_lse_ag_out_rs-style gather: vLLM-Ascend "Context Parallel (CP)", DCP
+ * decode; weights from the blockwise decomposition of the "Ring Attention"
+ * tag page):  LSE = ln sum_p e^{LSE_p},  O = sum_p e^{LSE_p - LSE} O_p.
+ * A partial with LSE_p = -inf has weight 0 and its O_p is not read; if every
+ * partial is -inf the result is O = 0, LSE = -inf.
+ *
+ * o_parts   device float [P, T, H, d]; lse_parts device float [P, T, H].
+ * o_out     device [T, H, d] out in out_dt; lse_out device float [T, H] out
+ *           (may be NULL).  Requires P >= 1, d % 4 == 0, 16-byte aligned.
+ * ---------------------------------------------------------------------- */
+ra_status ra_lse_merge(const float* o_parts, const float* lse_parts, int32_t P, int64_t T,
+                       int32_t H, int32_t d, void* o_out, ra_dtype out_dt, float* lse_out,
+                       ra_stream stream);
+
+/* ------------------------------------------------------------------------
+ * ra_cp_slot_mapping -- interleaved context-parallel KV-cache slot mapping.
+ * Source: vLLM-Ascend "Context Parallel (CP)", section "Block table":
+ * V = block_size*pcp*dcp; for token position x: vb = x / V, o = x % V,
+ * lbi = o / interleave, device = lbi % (pcp*dcp),
+ * offset = (lbi / (pcp*dcp))*interleave + o % interleave,
+ * slot = block_table[request][vb]*block_size + offset on that device.
+ *
+ * query_start_loc device int32 [R+1]: tokens of request q are
+ *                 [query_start_loc[q], query_start_loc[q+1]) (non-decreasing,
+ *                 query_start_loc[0] = 0, query_start_loc[R] = T).
+ * positions       device int32 [T]: position x of each token in its request.
+ * block_table     device int32 [R, max_vblocks]: physical block id of each
+ *                 virtual block (the same id is used in every device's pool).
+ * slot_out        device int32 [pcp*dcp, T] out: slot on each device, -1 where
+ *                 the device does not store the token.
+ * Errors: block_size % interleave != 0 -> RA_ERR_INVALID_ARG (the page's
+ * rule); a token whose virtual block is >= max_vblocks or whose block id is
+ * negative -> RA_ERR_DEVICE_BOUNDS (slot -1 everywhere).
+ * ---------------------------------------------------------------------- */
+ra_status ra_cp_slot_mapping(const int32_t* query_start_loc, const int32_t* positions,
+                             const int32_t* block_table, int32_t max_vblocks, int32_t R,
+                             int64_t T, int32_t block_size, int32_t interleave, int32_t pcp,
+                             int32_t dcp, int32_t* slot_out, ra_stream stream);
+
+/* ------------------------------------------------------------------------
+ * ra_cp_kv_scatter -- write token K/V rows into the sharded paged cache at the
+ * slots of ra_cp_slot_mapping (the cache write that slot_mapping drives).
+ *
+ * k, v      device [T, Hkv, d] (dtype dt).
+ * slot      device int32 [W, T] from ra_cp_slot_mapping (W = pcp*dcp).
+ * k_cache, v_cache device [W, num_blocks, Hkv, block_size, d] (dtype dt):
+ *           device w, block b, head g, in-block slot s is one d-vector.
+ * A slot outside [0, num_blocks*block_size) is a device bounds error.
+ * ---------------------------------------------------------------------- */
+ra_status ra_cp_kv_scatter(const void* k, const void* v, const int32_t* slot, void* k_cache,
+                           void* v_cache, int64_t T, int32_t W, int32_t Hkv, int32_t d,
+                           int32_t block_size, int64_t num_blocks, ra_dtype dt, ra_stream stream);
+
+/* ------------------------------------------------------------------------
+ * ra_cp_decode -- one-token decode over the sharded paged cache: split-KV
+ * partials per (request, device, split) followed by ra_lse_merge.
+ * Source: vLLM-Ascend "Context Parallel (CP)", DCP decode and PCP decode
+ * (attention over the local KV shard, then cp_lse_ag_out_rs); on one GPU all
+ * W = pcp*dcp devices are virtual and every partial is merged at once.
+ *
+ * q           device bf16 [R, Hq, d] (the query token of each request).
+ * k_cache, v_cache device bf16 [W, num_blocks, Hkv, block_size, d].
+ * block_table device int32 [R, max_vblocks]; ctx_lens device int32 [R]: the
+ *             query of request r attends its tokens 0..ctx_lens[r]-1.
+ * split_blocks virtual blocks per split (>= 1): partial p = w*n_splits + s
+ *             covers device w's blocks of virtual blocks
+ *             [s*split_blocks, (s+1)*split_blocks), n_splits =
+ *             ceil(max_vblocks/split_blocks).
+ * o           device [R, Hq, d] out (out_dt); lse device float [R, Hq] out
+ *             (may be NULL).
+ * workspace   device scratch of ra_cp_decode_workspace_size() bytes
+ *             (16-byte aligned): the fp32 partials.
+ * Requires d in {64,128}, Hq % Hkv == 0, Hq/Hkv <= 8,
+ * block_size % interleave == 0, every ctx_lens[r] <= max_vblocks*V.
+ * ---------------------------------------------------------------------- */
+ra_status ra_cp_decode_workspace_size(int32_t R, int32_t Hq, int32_t d, int32_t max_vblocks,
+                                      int32_t pcp, int32_t dcp, int32_t split_blocks,
+                                      size_t* bytes);
+
+ra_status ra_cp_decode(const void* q, const void* k_cache, const void* v_cache,
+                       const int32_t* block_table, const int32_t* ctx_lens, int32_t R,
+                       int32_t Hq, int32_t Hkv, int32_t d, int32_t block_size,
+                       int32_t interleave, int32_t pcp, int32_t dcp, int32_t max_vblocks,
+                       int64_t num_blocks, float scale, int32_t split_blocks, void* o,
+                       ra_dtype out_dt, float* lse, void* workspace, size_t ws_bytes,
+                       ra_stream stream);
+
+/* ------------------------------------------------------------------------
+ * Self-test of the bounded-wait machinery: launches one CTA that waits on an
+ * mbarrier nobody arrives at, for at most `limit_cycles` SM clock cycles,
+ * then records RA_ERR_TIMEOUT in the device error word and returns.  The
+ * context stays usable.  Used by the tests to check failure detection.
+ * ---------------------------------------------------------------------- */
+ra_status ra_selftest_wait_timeout(int64_t limit_cycles, ra_stream stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RINGATTN_H */

@@ -1,0 +1,117 @@
+"""CPU-side checks of the C ABI: the library loads, exports every function the
+headers declare, and rejects invalid arguments on the host (no GPU needed:
+validation happens before any CUDA call)."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def ra():
+    from context_long_sequence_ring_gb300 import build, ringattn
+    if not os.path.exists(build.LIB):
+        build.build()
+    return ringattn
+
+
+def _declared():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = open(h).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        names |= set(re.findall(r"\b(ra_[a-z0-9_]+)\s*\(", src))
+    return names
+
+
+def test_headers_declare_the_boundary():
+    names = _declared()
+    for n in ["ra_zigzag_partition", "ra_gather_rows", "ra_ring_attn_fwd", "ra_lse_merge", "ra_cp_slot_mapping",
+              "ra_cp_kv_scatter", "ra_cp_decode", "ra_cp_decode_workspace_size", "ra_device_status",
+              "ra_last_error"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(ra):
+    L = ctypes.CDLL(ra.LIB)
+    missing = [n for n in sorted(_declared()) if not hasattr(L, n)]
+    assert not missing, missing
+    # and the binding knows every declared function
+    known = set(ra.SIGNATURES) | set(ra.STRING_FUNCS)
+    assert _declared() <= known, _declared() - known
+
+
+def test_version_and_empty_error(ra):
+    assert "sm_103a" in ra.version()
+    assert ra.last_error() == ""
+
+
+def _call(ra, name, *args):
+    return getattr(ra.lib(), name)(*args)
+
+
+def test_attention_argument_validation(ra):
+    p = ctypes.c_void_p(16)  # never dereferenced: validation fails first
+    base = dict(B=1, Hq=4, Hkv=2, S=256, d=128, dt=1, causal=1, N=2, scale=0.0, layout=0)
+
+    def run(**kw):
+        a = dict(base, **kw)
+        return _call(ra, "ra_ring_attn_fwd", p, p, p, p, p, a["B"], a["Hq"], a["Hkv"], a["S"], a["d"], a["dt"],
+                     a["causal"], a["N"], a["scale"], a["layout"], None)
+
+    assert run(Hq=3) == ra.RA_ERR_INVALID_ARG and "multiple of Hkv" in ra.last_error()
+    assert run(S=250) == ra.RA_ERR_INVALID_ARG and "2*n_ranks" in ra.last_error()
+    assert run(N=0) == ra.RA_ERR_INVALID_ARG
+    assert run(d=96) == ra.RA_ERR_UNSUPPORTED
+    assert run(layout=7) == ra.RA_ERR_INVALID_ARG
+    assert run(dt=5) == ra.RA_ERR_INVALID_ARG
+    q = ctypes.c_void_p(24)  # misaligned
+    assert _call(ra, "ra_ring_attn_fwd", q, p, p, p, p, 1, 4, 2, 256, 128, 1, 1, 2, 0.0, 0, None) == \
+        ra.RA_ERR_INVALID_ARG
+
+
+def test_slot_mapping_rejects_bad_interleave(ra):
+    p = ctypes.c_void_p(16)
+    st = _call(ra, "ra_cp_slot_mapping", p, p, p, 4, 1, 10, 100, 16, 2, 4, p, None)
+    assert st == ra.RA_ERR_INVALID_ARG and "interleave" in ra.last_error()
+
+
+def test_decode_validation_and_workspace(ra):
+    n = ra.cp_decode_workspace_size(64, 32, 128, 129, 2, 4, 8)
+    P = 8 * 17
+    assert n >= P * 64 * 32 * 128 * 4 + P * 64 * 32 * 4
+    p = ctypes.c_void_p(16)
+    st = _call(ra, "ra_cp_decode", p, p, p, p, p, 2, 32, 8, 128, 100, 16, 2, 4, 4, 16, 0.0, 2, p, 1, p, p, 1 << 30,
+               None)
+    assert st == ra.RA_ERR_INVALID_ARG
+    st = _call(ra, "ra_cp_decode", p, p, p, p, p, 2, 32, 8, 96, 128, 16, 2, 4, 4, 16, 0.0, 2, p, 1, p, p, 1 << 30,
+               None)
+    assert st == ra.RA_ERR_UNSUPPORTED
+    st = _call(ra, "ra_cp_decode", p, p, p, p, p, 2, 32, 8, 128, 128, 16, 2, 4, 4, 16, 0.0, 2, p, 1, p, p, 16, None)
+    assert st == ra.RA_ERR_INVALID_ARG and "workspace" in ra.last_error()
+
+
+def test_zigzag_size_query_without_device(ra):
+    lens = (ctypes.c_int64 * 2)(8, 5)
+    G, T = ctypes.c_int64(0), ctypes.c_int64(0)
+    assert _call(ra, "ra_zigzag_partition", lens, 2, 2, None, None, ctypes.byref(G), ctypes.byref(T), None) == 0
+    assert (G.value, T.value) == (16, 13)
+    bad = (ctypes.c_int64 * 1)(-1)
+    assert _call(ra, "ra_zigzag_partition", bad, 1, 2, None, None, None, None, None) == ra.RA_ERR_INVALID_ARG
+
+
+def test_merge_validation(ra):
+    p = ctypes.c_void_p(16)
+    assert _call(ra, "ra_lse_merge", p, p, 0, 4, 2, 8, p, 0, p, None) == ra.RA_ERR_INVALID_ARG
+    assert _call(ra, "ra_lse_merge", p, p, 2, 4, 2, 6, p, 0, p, None) == ra.RA_ERR_UNSUPPORTED
+
+
+def test_product_path_has_no_oracle_or_fallback():
+    pkg = os.path.join(ROOT, "context_long_sequence_ring_gb300")
+    for f in glob.glob(os.path.join(pkg, "*.py")) + glob.glob(os.path.join(pkg, "csrc", "*")):
+        src = open(f).read()
+        assert "import oracle" not in src and "from oracle" not in src, f

@@ -1,0 +1,185 @@
+"""GPU parity of ring-order attention (C ABI) against the float64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from context_long_sequence_ring_gb300 import inputs as I
+from tests._gpu import ra_lib, assert_parity, check_status, TOL
+
+pytestmark = [pytest.mark.gpu, pytest.mark.filterwarnings("ignore::RuntimeWarning")]
+
+
+@pytest.fixture(scope="module")
+def ra():
+    return ra_lib()
+
+
+def _run(ra, seed, B, S, Hq, Hkv, d, N, causal, dtype, layout="natural"):
+    q, k, v = I.prefill_inputs(seed, B, S, Hq, Hkv, d, dtype)
+    dev = torch.device("cuda")
+    if layout == "natural":
+        o, lse = ra.ring_attn_fwd(q.to(dev), k.to(dev), v.to(dev), causal, N, B=B)
+    else:
+        perm, restore = ra.zigzag_partition([S] * B, N)
+        qz, kz, vz = (ra.gather_rows(x.to(dev), perm) for x in (q, k, v))
+        oz, lz = ra.ring_attn_fwd(qz, kz, vz, causal, N, B=B, layout="zigzag")
+        o, lse = ra.gather_rows(oz, restore), ra.gather_rows(lz, restore)
+    check_status(ra)
+    return q, k, v, o, lse
+
+
+def _oracle_full(q, k, v, B, S, causal):
+    Os, Ls = [], []
+    for b in range(B):
+        O, L = oracle.full_attention(q[b * S:(b + 1) * S], k[b * S:(b + 1) * S], v[b * S:(b + 1) * S], causal)
+        Os.append(O)
+        Ls.append(L)
+    return np.concatenate(Os), np.concatenate(Ls)
+
+
+# --------------------------------------------------------------------- tiny fp32 (exact path)
+
+@pytest.mark.parametrize("layout", ["natural", "zigzag"])
+def test_tiny_fp32_non_causal_four_ranks(ra, layout):
+    """B=1, Hq=Hkv=2, S=256, d=64, fp32 N(0,1), non-causal, N=4 ranks of 64 tokens."""
+    q, k, v, o, lse = _run(ra, 1, 1, 256, 2, 2, 64, 4, False, torch.float32, layout)
+    O, L = oracle.full_attention(q, k, v, False)
+    assert_parity(o, O, lse, L, torch.float32, "tiny fp32")
+
+
+@pytest.mark.parametrize("S,N,causal,Hq,Hkv,d", [(96, 3, True, 4, 2, 128), (200, 2, True, 3, 1, 64),
+                                                  (64, 1, False, 2, 2, 128)])
+def test_fp32_ragged_and_gqa(ra, S, N, causal, Hq, Hkv, d):
+    q, k, v, o, lse = _run(ra, 7, 2, S, Hq, Hkv, d, N, causal, torch.float32)
+    O, L = _oracle_full(q, k, v, 2, S, causal)
+    assert_parity(o, O, lse, L, torch.float32, "fp32 S=%d" % S)
+
+
+# --------------------------------------------------------------------- bf16 tensor-core path
+
+@pytest.mark.parametrize("S,N,B,Hq,Hkv,d,causal", [
+    (512, 2, 1, 2, 2, 128, True),      # chunks of 128: tile-aligned
+    (640, 2, 2, 4, 2, 128, True),      # chunks of 160: ragged last tile
+    (1200, 3, 1, 4, 1, 128, True),     # chunks of 200, GQA group 4
+    (640, 2, 1, 4, 2, 128, False),     # non-causal
+    (768, 4, 1, 2, 1, 64, True),       # d = 64, chunks of 96 (single ragged tile)
+    (2048, 4, 1, 2, 2, 64, False),
+    (16, 8, 1, 2, 2, 128, True),       # chunks of 1 token
+])
+def test_bf16_parity_small(ra, S, N, B, Hq, Hkv, d, causal):
+    q, k, v, o, lse = _run(ra, 3, B, S, Hq, Hkv, d, N, causal, torch.bfloat16)
+    O, L = _oracle_full(q, k, v, B, S, causal)
+    assert_parity(o, O, lse, L, torch.bfloat16, "bf16 S=%d N=%d" % (S, N))
+
+
+def test_bf16_zigzag_layout_is_bitwise_natural(ra):
+    B, S, Hq, Hkv, d, N = 2, 1280, 4, 2, 128, 4
+    _, _, _, o1, l1 = _run(ra, 5, B, S, Hq, Hkv, d, N, True, torch.bfloat16, "natural")
+    _, _, _, o2, l2 = _run(ra, 5, B, S, Hq, Hkv, d, N, True, torch.bfloat16, "zigzag")
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_bf16_causal_prefill_8k_full(ra):
+    """B=1, Hq=Hkv=8, S=8192, d=128, causal, N=8 (16 chunks of 512), every output checked."""
+    q, k, v, o, lse = _run(ra, 2, 1, 8192, 8, 8, 128, 8, True, torch.bfloat16)
+    O, L = oracle.full_attention(q, k, v, True)
+    assert_parity(o, O, lse, L, torch.bfloat16, "8k causal")
+
+
+def _sample_rows(S, N, c, rng, n_random):
+    rows = set()
+    for ch in range(2 * N):
+        for off in (0, 1, 127, 128, c - 1):
+            if 0 <= off < c:
+                rows.add(ch * c + off)
+    rows |= set(rng.integers(0, S, size=n_random).tolist())
+    return np.array(sorted(rows))
+
+
+def _device_inputs(ra, seed, B, S, Hq, Hkv, d):
+    tab = I.normal_table(torch.bfloat16)
+    q = ra.synth_fill(I.tensor_key(seed, I.TID_Q), tab, (B * S, Hq, d))
+    k = ra.synth_fill(I.tensor_key(seed, I.TID_K), tab, (B * S, Hkv, d))
+    v = ra.synth_fill(I.tensor_key(seed, I.TID_V), tab, (B * S, Hkv, d))
+    return q, k, v
+
+
+def _check_sampled(o, lse, seed, b, S, Hq, Hkv, d, rows, causal=True):
+    base = b * S
+    qr = I.synth_rows(seed, I.TID_Q, base + rows, Hq * d, torch.bfloat16).reshape(len(rows), Hq, d)
+    kk = I.synth_rows(seed, I.TID_K, base + np.arange(S), Hkv * d, torch.bfloat16).reshape(S, Hkv, d)
+    vv = I.synth_rows(seed, I.TID_V, base + np.arange(S), Hkv * d, torch.bfloat16).reshape(S, Hkv, d)
+    O, L = oracle.attention_rows(qr, rows, kk, vv, causal)
+    idx = torch.as_tensor(base + rows, device=o.device)
+    return assert_parity(o[idx], O, lse[idx], L, torch.bfloat16, "sampled rows seq %d" % b)
+
+
+def test_device_generator_matches_host(ra):
+    tab = I.normal_table(torch.bfloat16)
+    key = I.tensor_key(9, I.TID_K)
+    x = ra.synth_fill(key, tab, (1 << 20,))
+    idx = np.arange(1 << 20)
+    assert torch.equal(x.cpu(), I.synth_normal_at(9, I.TID_K, idx, torch.bfloat16))
+
+
+def test_bf16_gqa_32k_zigzag_with_restore_round_trip(ra):
+    """B=2, Hq=32, Hkv=8, S=32768, d=128, causal, N=8 zigzag ranks (16 chunks of 2048),
+    tile 128; inputs permuted to the gathered layout, outputs restored; sampled rows."""
+    B, S, Hq, Hkv, d, N, seed = 2, 32768, 32, 8, 128, 8, 3
+    q, k, v = _device_inputs(ra, seed, B, S, Hq, Hkv, d)
+    perm, restore = ra.zigzag_partition([S] * B, N)
+    qz, kz, vz = (ra.gather_rows(x, perm) for x in (q, k, v))
+    assert torch.equal(ra.gather_rows(qz, restore), q)          # restore o perm = identity, bit-exact
+    oz, lz = ra.ring_attn_fwd(qz, kz, vz, True, N, B=B, layout="zigzag")
+    o, lse = ra.gather_rows(oz, restore), ra.gather_rows(lz, restore)
+    check_status(ra)
+    rng = np.random.default_rng(33)
+    c = S // (2 * N)
+    for b in range(B):
+        _check_sampled(o, lse, seed, b, S, Hq, Hkv, d, _sample_rows(S, N, c, rng, 32))
+
+
+def test_bf16_long_context_131k(ra):
+    """B=1, Hq=32, Hkv=8, S=131072, d=128, causal, N=16 (32 chunks of 4096); sampled rows."""
+    B, S, Hq, Hkv, d, N, seed = 1, 131072, 32, 8, 128, 16, 5
+    q, k, v = _device_inputs(ra, seed, B, S, Hq, Hkv, d)
+    o, lse = ra.ring_attn_fwd(q, k, v, True, N, B=B)
+    check_status(ra)
+    rng = np.random.default_rng(55)
+    rows = _sample_rows(S, N, S // (2 * N), rng, 16)
+    rows = np.concatenate([rows[::3], [0, S - 1]])
+    _check_sampled(o, lse, seed, 0, S, Hq, Hkv, d, np.unique(rows))
+
+
+# --------------------------------------------------------------------- schedule
+
+@pytest.mark.parametrize("S,N", [(512, 2), (640, 2), (8192, 8), (1200, 3), (16, 8), (2 * 16 * 300, 16)])
+def test_schedule_counts_match_brute_force(ra, S, N):
+    c = S // (2 * N)
+    got = ra.ring_schedule_counts(S, N, True).cpu().tolist()
+    check_status(ra)
+    assert got == [list(x) for x in oracle.causal_tiles_per_rank(N, c, 128)]
+    nt = -(-c // 128)
+    got_nc = ra.ring_schedule_counts(S, N, False).cpu().tolist()
+    assert got_nc == [[2 * nt * 2 * N * nt, 0, 0]] * N
+
+
+# --------------------------------------------------------------------- failure detection
+
+def test_bounded_wait_times_out_and_context_survives(ra):
+    ra.selftest_wait_timeout(1 << 20)
+    st = ra.device_status()
+    assert st == ra.RA_ERR_TIMEOUT, (st, ra.last_error())
+    assert ra.device_status() == 0          # cleared
+    # the context is still usable
+    q, k, v, o, lse = _run(ra, 1, 1, 256, 2, 2, 64, 4, False, torch.float32)
+    O, L = oracle.full_attention(q, k, v, False)
+    assert_parity(o, O, lse, L, torch.float32, "after timeout")
+
+
+def test_invalid_arguments_raise(ra):
+    q = torch.zeros((250, 2, 128), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(ra.RingAttnError):
+        ra.ring_attn_fwd(q, q, q, True, 4)
+    assert TOL  # tolerance table is shared with the other GPU tests
