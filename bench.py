@@ -1,0 +1,479 @@
+"""Benchmark of the ring-order attention hot path on GB300.
+
+One step = one pass of the whole path over one batch of synthetic input:
+  prefill (B=1, Hq=32, Hkv=8, S=131072, d=128, bf16, causal, N=16 virtual ranks):
+    zigzag partition -> gather Q/K/V into the ranks' head-tail layout ->
+    ring-order attention -> restore O and LSE to token order;
+  decode (64 requests, context U[4096, 131072], Hq=32, Hkv=8, d=128, bf16,
+    block 128, interleave 16, pcp=2, dcp=4): slot mapping + cache write of the
+    new token of every request -> split-KV partials -> LSE merge.
+
+Prints one JSON line.  ``value`` is causal-adjusted attention TFLOP/s over the
+whole timed step (prefill + decode); the decode+merge GB/s and the per-kernel
+rooflines are reported beside it.  ``--impl reference`` times the float64
+oracle instead (a bounded sample per step on the host cores).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from context_long_sequence_ring_gb300 import inputs as I  # noqa: E402
+
+METRIC = "ring-attn fwd TFLOP/s (causal-adj) & % bf16 peak; decode+merge GB/s % HBM"
+PREFILL = dict(B=1, Hq=32, Hkv=8, S=131072, d=128, N=16, seed=5)
+DECODE = dict(R=64, lo=4096, hi=131072, Hq=32, Hkv=8, d=128, bs=128, I=16, pcp=2, dcp=4, seed=4, split=8)
+KERNEL_SOURCES = {"ring_attn_bf16": "ra_attn_bf16.cu", "cp_decode": "ra_decode.cu"}
+
+
+def causal_flops(B, Hq, S, d):
+    """Algorithmic FLOPs of causal attention forward: QK^T and PV, 2 per MAC."""
+    return 4.0 * B * Hq * d * S * (S + 1) / 2
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            m = json.load(f)
+        return dict(hbm=m["hbm_gbs"], bf16=m["bf16_tflops"], bf16_sus=m["bf16_tflops_sustained"], src="measured")
+    except Exception:
+        return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+
+
+def _source_hash(name):
+    p = os.path.join(ROOT, "context_long_sequence_ring_gb300", "csrc", name)
+    with open(p, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def _traffic(kernel):
+    """DRAM bytes per launch from the committed ncu summary, if it is for this source."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            t = json.load(f)[kernel]
+        if t.get("source_sha256_16") != _source_hash(KERNEL_SOURCES[kernel]):
+            return None
+        return t["dram_bytes_per_launch"]
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        rows = [r.split(",") for r in (self.out or "").strip().splitlines() if r.count(",") >= 8]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].strip().lower() == "active"})
+        pw = [float(r[3]) for r in rows if r[3].strip().replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows), "power_w_max": max(pw) if pw else None}
+
+
+# ---------------------------------------------------------------------------- our arm
+
+class Workload:
+    def __init__(self, ra, dev, parts=("prefill", "decode")):
+        self.ra, self.dev = ra, dev
+        self.parts = parts
+        P, D = PREFILL, DECODE
+        tab = I.normal_table(torch.bfloat16)
+        self.launches_per_step = 0
+        if "prefill" in parts:
+            self._init_prefill(tab)
+            self.launches_per_step += 7
+        if "decode" in parts:
+            self._init_decode(tab)
+            self.launches_per_step += 4
+        torch.cuda.synchronize()
+
+    def _init_prefill(self, tab):
+        ra, dev, P = self.ra, self.dev, PREFILL
+        n = P["B"] * P["S"]
+        self.q = ra.synth_fill(I.tensor_key(P["seed"], I.TID_Q), tab, (n, P["Hq"], P["d"]), dev)
+        self.k = ra.synth_fill(I.tensor_key(P["seed"], I.TID_K), tab, (n, P["Hkv"], P["d"]), dev)
+        self.v = ra.synth_fill(I.tensor_key(P["seed"], I.TID_V), tab, (n, P["Hkv"], P["d"]), dev)
+        self.seq_lens = [P["S"]] * P["B"]
+        self.perm = torch.empty(n, dtype=torch.int32, device=dev)
+        self.restore = torch.empty(n, dtype=torch.int32, device=dev)
+        self.qz, self.kz, self.vz = (torch.empty_like(x) for x in (self.q, self.k, self.v))
+        self.oz = torch.empty_like(self.q)
+        self.lz = torch.empty((n, P["Hq"]), dtype=torch.float32, device=dev)
+        self.o = torch.empty_like(self.q)
+        self.lse = torch.empty_like(self.lz)
+
+    def _init_decode(self, tab):
+        # cache filled once (slot mapping + scatter of every context token)
+        ra, dev, D = self.ra, self.dev, DECODE
+        wl = I.decode_workload(D["seed"], D["R"], D["lo"], D["hi"], D["bs"], D["pcp"], D["dcp"])
+        self.wl = wl
+        W = D["pcp"] * D["dcp"]
+        T = wl["total_tokens"]
+        kt = ra.synth_fill(I.tensor_key(D["seed"], I.TID_K), tab, (T, D["Hkv"], D["d"]), dev)
+        vt = ra.synth_fill(I.tensor_key(D["seed"], I.TID_V), tab, (T, D["Hkv"], D["d"]), dev)
+        ctx = wl["ctx_lens"]
+        qsl = torch.zeros(D["R"] + 1, dtype=torch.int32)
+        qsl[1:] = torch.cumsum(ctx, 0)
+        pos = torch.cat([torch.arange(int(L), dtype=torch.int32) for L in ctx])
+        self.bt = wl["block_table"].to(dev)
+        self.ctx = ctx.to(dev)
+        slot = ra.cp_slot_mapping(qsl.to(dev), pos.to(dev), self.bt, D["bs"], D["I"], D["pcp"], D["dcp"])
+        self.kc = torch.empty((W, wl["num_blocks"], D["Hkv"], D["bs"], D["d"]), dtype=torch.bfloat16, device=dev)
+        self.vc = torch.empty_like(self.kc)
+        ra.cp_kv_scatter(kt, vt, slot, self.kc, self.vc)
+        # the step's new tokens: the last token of every request (position L-1)
+        last = (qsl[1:] - 1).long()
+        self.new_k = kt[last.to(dev)].contiguous()
+        self.new_v = vt[last.to(dev)].contiguous()
+        del kt, vt, slot
+        self.new_pos = (ctx - 1).to(torch.int32).to(dev)
+        self.new_qsl = torch.arange(D["R"] + 1, dtype=torch.int32, device=dev)
+        self.new_slot = torch.empty((W, D["R"]), dtype=torch.int32, device=dev)
+        self.qd = I.synth_normal(D["seed"], I.TID_Q, (D["R"], D["Hq"], D["d"]), torch.bfloat16).to(dev)
+        self.od = torch.empty((D["R"], D["Hq"], D["d"]), dtype=torch.bfloat16, device=dev)
+        self.ld = torch.empty((D["R"], D["Hq"]), dtype=torch.float32, device=dev)
+        ws = ra.cp_decode_workspace_size(D["R"], D["Hq"], D["d"], wl["max_vblocks"], D["pcp"], D["dcp"], D["split"])
+        self.ws = torch.empty(ws, dtype=torch.uint8, device=dev)
+
+    def decode_bytes(self):
+        D = self.ctx.cpu().numpy().astype(np.int64)
+        P = DECODE
+        W = P["pcp"] * P["dcp"]
+        vbs = P["bs"] * W
+        kv = int(D.sum()) * P["Hkv"] * P["d"] * 2 * 2
+        nvb = -(-D // vbs)
+        live = int(np.sum(W * (-(-nvb // P["split"]))))            # partials written and read once
+        part = live * P["Hq"] * (P["d"] + 1) * 4 * 2
+        q_o = 2 * P["R"] * P["Hq"] * P["d"] * 2
+        return kv + part + q_o, kv
+
+    def step(self, events=None):
+        ra, P, D = self.ra, PREFILL, DECODE
+        e = events
+        if e: e[0].record()
+        if "prefill" not in self.parts:
+            for i in (1, 2, 3):
+                if e: e[i].record()
+        else:
+            self._prefill(e)
+        if "decode" not in self.parts:
+            for i in (4, 5):
+                if e: e[i].record()
+        else:
+            self._decode(e)
+
+    def _prefill(self, e):
+        ra, P = self.ra, PREFILL
+        # a1: head-tail partition of the batch (device kernel), a2: gather to rank-major layout
+        ra.lib().ra_zigzag_partition((ra._c.c_int64 * 1)(P["S"]), 1, P["N"], self.perm.data_ptr(),
+                                     self.restore.data_ptr(), None, None, ra._stream())
+        ra.gather_rows(self.q, self.perm, self.qz)
+        ra.gather_rows(self.k, self.perm, self.kz)
+        ra.gather_rows(self.v, self.perm, self.vz)
+        if e: e[1].record()
+        # a3-a5: ring-order attention over the N virtual ranks
+        ra.ring_attn_fwd(self.qz, self.kz, self.vz, True, P["N"], B=P["B"], layout="zigzag", o=self.oz, lse=self.lz)
+        if e: e[2].record()
+        # a2: restore token order
+        ra.gather_rows(self.oz, self.restore, self.o)
+        ra.gather_rows(self.lz, self.restore, self.lse)
+        if e: e[3].record()
+
+    def _decode(self, e):
+        ra, D = self.ra, DECODE
+        # a6: slot mapping + cache write of the new tokens; a7: split-KV decode; a8: LSE merge
+        ra.cp_slot_mapping(self.new_qsl, self.new_pos, self.bt, D["bs"], D["I"], D["pcp"], D["dcp"], out=self.new_slot)
+        ra.cp_kv_scatter(self.new_k, self.new_v, self.new_slot, self.kc, self.vc)
+        if e: e[4].record()
+        ra.cp_decode(self.qd, self.kc, self.vc, self.bt, self.ctx, D["I"], D["pcp"], D["dcp"], split_blocks=D["split"],
+                     workspace=self.ws, o=self.od, lse=self.ld)
+        if e: e[5].record()
+
+
+def run_ours(args, rank, world, dev):
+    from context_long_sequence_ring_gb300 import ringattn as ra
+    ra.lib()
+    wl = Workload(ra, dev)
+    P = PREFILL
+    for _ in range(args.warmup):
+        wl.step()
+    torch.cuda.synchronize()
+    st = ra.device_status()
+    if st != 0:
+        raise RuntimeError("device status %d after warm-up: %s" % (st, ra.last_error()))
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    _barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+        t_start.record()
+        for i in range(args.steps):
+            wl.step(evs[i])
+        t_end.record()
+        torch.cuda.synchronize()
+    _barrier(world)
+    ms_total = t_start.elapsed_time(t_end)
+    ms_total = _max_over_ranks(ms_total, world, dev)
+    st = ra.device_status()
+    if st != 0:
+        raise RuntimeError("device status %d after timing: %s" % (st, ra.last_error()))
+    attn_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    prefill_ms = statistics.mean(e[0].elapsed_time(e[3]) for e in evs)
+    decode_kernel_ms = statistics.mean(e[4].elapsed_time(e[5]) for e in evs)
+    decode_ms = statistics.mean(e[3].elapsed_time(e[5]) for e in evs)
+    flops = causal_flops(P["B"], P["Hq"], P["S"], P["d"])
+    dec_bytes, kv_bytes = wl.decode_bytes()
+    pk = _peaks()
+    ms_step = ms_total / args.steps
+    value = world * flops / (ms_step * 1e-3) / 1e12
+
+    # e2e through the public API from pinned host buffers: H2D Q/K/V and the decode step's
+    # inputs, the full step, D2H of O/LSE and the decode output.
+    hq, hk, hv = (x.cpu().pin_memory() for x in (wl.q, wl.k, wl.v))
+    hqd, hnk, hnv = (x.cpu().pin_memory() for x in (wl.qd, wl.new_k, wl.new_v))
+    ho, hl = torch.empty_like(hq).pin_memory(), torch.empty_like(wl.lse, device="cpu").pin_memory()
+    hod, hld = torch.empty_like(hqd).pin_memory(), torch.empty_like(wl.ld, device="cpu").pin_memory()
+    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hqd, hnk, hnv))
+    d2h = sum(x.numel() * x.element_size() for x in (ho, hl, hod, hld))
+    e2e_steps = max(1, min(args.steps, 5))
+    _barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(e2e_steps):
+        wl.q.copy_(hq, non_blocking=True); wl.k.copy_(hk, non_blocking=True); wl.v.copy_(hv, non_blocking=True)
+        wl.qd.copy_(hqd, non_blocking=True); wl.new_k.copy_(hnk, non_blocking=True)
+        wl.new_v.copy_(hnv, non_blocking=True)
+        wl.step()
+        ho.copy_(wl.o, non_blocking=True); hl.copy_(wl.lse, non_blocking=True)
+        hod.copy_(wl.od, non_blocking=True); hld.copy_(wl.ld, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = _max_over_ranks(e0.elapsed_time(e1), world, dev) / e2e_steps
+    _barrier(world)
+
+    attn_tflops = flops / (attn_ms * 1e-3) / 1e12
+    dec_gbs = dec_bytes / (decode_kernel_ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded counter-based N(0,1), bf16)",
+        "config": {"workload": "causal GQA ring prefill B=1 Hq=32 Hkv=8 S=131072 d=128 N=16 zigzag ranks "
+                               "+ CP decode 64 req ctx U[4096,131072] Hq=32 Hkv=8 d=128 bs=128 I=16 pcp=2 dcp=4",
+                   "prefill": PREFILL, "decode": {k: v for k, v in DECODE.items()},
+                   "l2": "inputs larger than L2 (Q 1 GiB, K/V 256 MiB each, KV cache %.1f GB)" % (
+                       2 * wl.kc.numel() * 2 / 1e9),
+                   "parallelism": "replicas (one independent problem per GPU)" if world > 1 else "1 GPU"},
+        "parts": {
+            "prefill_ms": round(prefill_ms, 3), "ring_attn_kernel_ms": round(attn_ms, 3),
+            "ring_attn_tflops": round(attn_tflops, 1),
+            "decode_merge_ms": round(decode_kernel_ms, 4), "decode_step_ms": round(decode_ms, 4),
+            "decode_merge_gbs": round(dec_gbs, 1), "decode_kv_bytes": kv_bytes, "decode_alg_bytes": dec_bytes,
+        },
+        "roofline": {"bound": "tensor", "achieved": round(attn_tflops, 1), "peak": pk["bf16_sus"], "unit": "TFLOP/s",
+                     "frac": round(attn_tflops / pk["bf16_sus"], 4), "traffic": _traffic("ring_attn_bf16"),
+                     "kernel": "ring_attn_bf16_kernel", "peak_kind": "bf16 dense sustained (%s)" % pk["src"],
+                     "algorithmic": "%.4g FLOP per launch" % flops},
+        "roofline_decode": {"bound": "hbm", "achieved": round(dec_gbs, 1), "peak": pk["hbm"], "unit": "GB/s",
+                            "frac": round(dec_gbs / pk["hbm"], 4), "traffic": _traffic("cp_decode"),
+                            "kernel": "cp_decode_kernel + lse_merge_kernel", "peak_kind": "HBM copy (%s)" % pk["src"],
+                            "algorithmic": "%d bytes per step" % dec_bytes},
+        "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3)},
+        "gpu_launches": wl.launches_per_step * args.steps,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.cpu_rows)
+    return line
+
+
+def run_parts(args, dev):
+    """Run only some parts of the step (for profiler captures); prints part times, no headline."""
+    from context_long_sequence_ring_gb300 import ringattn as ra
+    parts = tuple(args.parts.split(","))
+    wl = Workload(ra, dev, parts)
+    for _ in range(args.warmup):
+        wl.step()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    for i in range(args.steps):
+        wl.step(evs[i])
+    torch.cuda.synchronize()
+    st = ra.device_status()
+    if st != 0:
+        raise RuntimeError("device status %d: %s" % (st, ra.last_error()))
+    out = {"parts": list(parts), "prefill": PREFILL if "prefill" in parts else None,
+           "ring_attn_kernel_ms": statistics.mean(e[1].elapsed_time(e[2]) for e in evs),
+           "decode_merge_ms": statistics.mean(e[4].elapsed_time(e[5]) for e in evs)}
+    if "prefill" in parts:
+        P = PREFILL
+        out["ring_attn_tflops"] = causal_flops(P["B"], P["Hq"], P["S"], P["d"]) / (out["ring_attn_kernel_ms"] * 1e-3) / 1e12
+    if "decode" in parts:
+        out["decode_merge_gbs"] = wl.decode_bytes()[0] / (out["decode_merge_ms"] * 1e-3) / 1e9
+    print(json.dumps(out), flush=True)
+
+
+# ---------------------------------------------------------------------------- oracle arm
+
+def _threads():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count()
+
+
+class OracleSample:
+    """The float64 oracle on a sample of query rows of the prefill workload."""
+
+    def __init__(self, rows_per_step):
+        P = PREFILL
+        S, Hkv, d = P["S"], P["Hkv"], P["d"]
+        self.k = I.synth_rows(P["seed"], I.TID_K, np.arange(S), Hkv * d, torch.bfloat16).reshape(S, Hkv, d)
+        self.v = I.synth_rows(P["seed"], I.TID_V, np.arange(S), Hkv * d, torch.bfloat16).reshape(S, Hkv, d)
+        self.k64 = self.k.double().numpy()
+        self.v64 = self.v.double().numpy()
+        self.rng = np.random.default_rng(77)
+        self.n = rows_per_step
+
+    def step(self):
+        import oracle
+        P = PREFILL
+        rows = np.sort(self.rng.integers(0, P["S"], size=self.n))
+        qr = I.synth_rows(P["seed"], I.TID_Q, rows, P["Hq"] * P["d"], torch.bfloat16).reshape(-1, P["Hq"], P["d"])
+        t0 = time.perf_counter()
+        oracle.attention_rows(qr, rows, self.k64, self.v64, True)
+        dt = time.perf_counter() - t0
+        flops = 4.0 * P["Hq"] * P["d"] * float(np.sum(rows + 1))     # causal pairs of the sampled rows
+        return flops, dt
+
+
+def cpu_baseline(rows):
+    s = OracleSample(rows)
+    s.step()  # warm
+    fl, dt = 0.0, 0.0
+    while dt < 10.0:
+        f, t = s.step()
+        fl += f
+        dt += t
+    return {"value": round(fl / dt / 1e12, 6), "unit": "TFLOP/s", "cores": _threads(), "kind": "oracle",
+            "sample": "%d random query rows x 32 heads of the S=131072 causal prefill per call, float64 numpy, "
+                      "%.1f s of CPU time" % (rows, dt)}
+
+
+def run_reference(args):
+    s = OracleSample(args.cpu_rows)
+    for _ in range(args.warmup):
+        s.step()
+    fl, dt = 0.0, 0.0
+    for _ in range(args.steps):
+        f, t = s.step()
+        fl += f
+        dt += t
+    value = fl / dt / 1e12
+    cb = {"value": round(value, 6), "unit": "TFLOP/s", "cores": _threads(), "kind": "oracle",
+          "sample": "%d random query rows x 32 heads per step of the S=131072 causal prefill, float64 numpy"
+                    % args.cpu_rows}
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 2),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "causal GQA ring prefill B=1 Hq=32 Hkv=8 S=131072 d=128 N=16 (sampled rows)",
+                       "prefill": PREFILL},
+            "cpu_baseline": cb,
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+# ---------------------------------------------------------------------------- driver
+
+def _barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def _max_over_ranks(x, world, dev):
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-rows", type=int, default=16)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--parts", default="all",
+                    help="'all' for the benchmark line, else 'prefill', 'decode' or 'prefill,decode' "
+                         "to run only those parts (profiler captures)")
+    ap.add_argument("--prefill-seq", type=int, default=None, help="override S of the prefill (multiple of 2N)")
+    args = ap.parse_args()
+    if args.prefill_seq:
+        PREFILL["S"] = args.prefill_seq
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if args.parts != "all":
+        run_parts(args, dev)
+        return
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=dev)
+    line = run_ours(args, rank, world, dev)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -429,6 +429,334 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
+// ===========================================================================
+// Two-head variant for GQA (Hq/Hkv even): a CTA runs two query heads that read
+// the same K/V head, so every K/V tile TMA brings in feeds two score tiles.
+// Roles (384 threads): warp 0 TMA, warp 1 TMEM allocation + MMA issue, warps
+// 4..7 softmax of head 0, warps 8..11 softmax of head 1 (warps 2, 3 idle).
+// Tensor memory: S_h = cols [128h, 128h+128), O_h = cols [256+128h, ...).
+// P_h (bf16, two per column) overwrites the first 64 columns of S_h and is
+// the A operand of O_h += P_h V straight from tensor memory, so P never
+// touches shared memory.  MMA issue order per K/V tile j:
+//   PV0_j, S0_{j+1}, PV1_j, S1_{j+1}
+// (tcgen05 operations of one thread execute in issue order, so S_h{j+1} may
+// overwrite the columns PV_h_j reads).  A softmax warpgroup only waits for
+// the previous P.V when it must rescale O (lazy rescale, threshold 2^8).
+// ===========================================================================
+struct Item2 {
+  int b, hq0, g, r, j;
+};
+__device__ __forceinline__ Item2 decode_item2(const Params& p, int idx) {
+  Item2 it;
+  const int pairs = p.group / 2;
+  const int hp = idx % pairs; idx /= pairs;
+  it.j = idx % p.nt; idx /= p.nt;
+  it.r = idx % p.N; idx /= p.N;
+  it.g = idx % p.Hkv; idx /= p.Hkv;
+  it.b = idx;
+  it.hq0 = it.g * p.group + 2 * hp;
+  return it;
+}
+
+template <int D>
+struct __align__(1024) Smem2 {
+  uint8_t q[2][BM * D * 2];
+  uint8_t k[STAGES][BN * D * 2];
+  uint8_t v[STAGES][BN * D * 2];
+  uint64_t q_full, q_empty, k_full[STAGES], k_empty[STAGES], v_full[STAGES], v_empty[STAGES];
+  uint64_t s_full[2], p_full[2], pv_done[2], o_empty[2], drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+constexpr int kThreads2 = 384;
+
+template <int D>
+__global__ void __launch_bounds__(kThreads2, 1)
+    ring_attn_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                               const __grid_constant__ CUtensorMap tmV, const Params p) {
+  constexpr int SLABS = D / 64;
+  constexpr uint32_t kTileBytes = BM * D * 2;
+  constexpr uint32_t kIdescS = idesc_bf16_f32(BM, BN, 0, 0);
+  constexpr uint32_t kIdescO = idesc_bf16_f32(BM, D, 0, 1);
+
+  extern __shared__ uint8_t smem_raw[];
+  Smem2<D>& sm = *reinterpret_cast<Smem2<D>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const Item2 it = decode_item2(p, blockIdx.x);
+  const Item it1{it.b, it.hq0, it.g, it.r, it.j};   // for tile_of()
+  const Sched sch{p.N, p.c, p.nt, p.causal};
+  volatile int* abort_flag = &sm.abort_flag;
+  const long long lim = p.wait_limit;
+
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&sm.q_full), 1);
+    mbar_init(smem_u32(&sm.q_empty), 1);
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_u32(&sm.k_full[s]), 1);
+      mbar_init(smem_u32(&sm.k_empty[s]), 1);
+      mbar_init(smem_u32(&sm.v_full[s]), 1);
+      mbar_init(smem_u32(&sm.v_empty[s]), 1);
+    }
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(smem_u32(&sm.s_full[h]), 1);
+      mbar_init(smem_u32(&sm.p_full[h]), 128);
+      mbar_init(smem_u32(&sm.pv_done[h]), 1);
+      mbar_init(smem_u32(&sm.o_empty[h]), 128);
+    }
+    mbar_init(smem_u32(&sm.drain), 1);
+    sm.abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&sm.tmem_base), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+
+  if (warp == 0) {
+    // ============================================================ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      uint32_t kv_cnt = 0;
+      bool issued[STAGES] = {false, false};
+      uint32_t last_ph[STAGES] = {0, 0};
+      bool ok = true;
+      for (int ti = 0; ti < 2 && ok; ++ti) {
+        int qc, qi;
+        tile_of(p, it1, ti, qc, qi);
+        if (!(ok = mbar_wait(smem_u32(&sm.q_empty), (ti & 1) ^ 1, abort_flag, lim, 101))) break;
+        const uint32_t qb = smem_u32(&sm.q_full);
+        mbar_arrive_expect_tx(qb, 2 * kTileBytes);
+        const int32_t qrow = static_cast<int32_t>(token_row(p, it.b, qc, qi * BM));
+        for (int h = 0; h < 2; ++h)
+          for (int s = 0; s < SLABS; ++s)
+            tma_load_3d(smem_u32(sm.q[h] + s * BM * 128), &tmQ, qb, 64 * s, it.hq0 + h, qrow);
+        KvIter kv;
+        kv.init(sch, qc, qi);
+        int kc, kt;
+        while (kv.next(kc, kt)) {
+          const int st = kv_cnt % STAGES;
+          const uint32_t ph = (kv_cnt / STAGES) & 1;
+          const int32_t krow = static_cast<int32_t>(token_row(p, it.b, kc, kt * BN));
+          if (!(ok = mbar_wait(smem_u32(&sm.k_empty[st]), ph ^ 1, abort_flag, lim, 102))) break;
+          mbar_arrive_expect_tx(smem_u32(&sm.k_full[st]), kTileBytes);
+          for (int s = 0; s < SLABS; ++s)
+            tma_load_3d(smem_u32(sm.k[st] + s * BN * 128), &tmK, smem_u32(&sm.k_full[st]), 64 * s, it.g, krow);
+          if (!(ok = mbar_wait(smem_u32(&sm.v_empty[st]), ph ^ 1, abort_flag, lim, 103))) break;
+          mbar_arrive_expect_tx(smem_u32(&sm.v_full[st]), kTileBytes);
+          for (int s = 0; s < SLABS; ++s)
+            tma_load_3d(smem_u32(sm.v[st] + s * BN * 128), &tmV, smem_u32(&sm.v_full[st]), 64 * s, it.g, krow);
+          issued[st] = true;
+          last_ph[st] = ph;
+          ++kv_cnt;
+        }
+      }
+      if (!ok) {
+        for (int s = 0; s < STAGES; ++s)
+          if (issued[s]) {
+            mbar_wait(smem_u32(&sm.k_full[s]), last_ph[s], abort_flag, 1 << 22, 0);
+            mbar_wait(smem_u32(&sm.v_full[s]), last_ph[s], abort_flag, 1 << 22, 0);
+          }
+      }
+    }
+  } else if (warp == 1) {
+    // ============================================================ MMA issuer
+    if (lane == 0) {
+      uint32_t kv_cnt = 0, pf_cnt[2] = {0, 0};
+      bool ok = true;
+      auto issue_s = [&](int h, int st) {
+        const uint32_t q_base = smem_u32(sm.q[h]), k_base = smem_u32(sm.k[st]);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
+          mma_bf16_ss(tmem + h * BN, desc_sw128(q_base + off, 16, 1024),
+                      desc_sw128(k_base + (kk >> 2) * (BN * 128) + (kk & 3) * 32, 16, 1024), kIdescS,
+                      kk > 0 ? 1u : 0u);
+        }
+        mma_commit(smem_u32(&sm.s_full[h]));
+      };
+      auto issue_pv = [&](int h, int st, bool first) {
+        const uint32_t v_base = smem_u32(sm.v[st]);
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)
+          mma_bf16_ts(tmem + kColO + h * D, tmem + h * BN + kk * 8, desc_sw128(v_base + kk * 16 * 128, BN * 128, 1024),
+                      kIdescO, (kk > 0 || !first) ? 1u : 0u);
+        mma_commit(smem_u32(&sm.pv_done[h]));
+      };
+      for (int ti = 0; ti < 2 && ok; ++ti) {
+        int qc, qi;
+        tile_of(p, it1, ti, qc, qi);
+        const int nkv = n_kv_tiles(sch, qc, qi);
+        if (!(ok = mbar_wait(smem_u32(&sm.q_full), ti & 1, abort_flag, lim, 110))) break;
+        // prologue: both score tiles of K/V tile 0
+        {
+          const int st = kv_cnt % STAGES;
+          if (!(ok = mbar_wait(smem_u32(&sm.k_full[st]), (kv_cnt / STAGES) & 1, abort_flag, lim, 111))) break;
+          tc_fence_after();
+          issue_s(0, st);
+          issue_s(1, st);
+          mma_commit(smem_u32(&sm.k_empty[st]));
+          if (nkv == 1) mma_commit(smem_u32(&sm.q_empty));
+        }
+        for (int j = 0; j < nkv && ok; ++j) {
+          const uint32_t c = kv_cnt + j;
+          const int st = c % STAGES;
+          const uint32_t ph = (c / STAGES) & 1;
+          const bool more = j + 1 < nkv;
+          const int st1 = (c + 1) % STAGES;
+          const uint32_t ph1 = ((c + 1) / STAGES) & 1;
+          // O_0 += P_0 V_j
+          if (!(ok = mbar_wait(smem_u32(&sm.p_full[0]), pf_cnt[0] & 1, abort_flag, lim, 112))) break;
+          ++pf_cnt[0];
+          if (!(ok = mbar_wait(smem_u32(&sm.v_full[st]), ph, abort_flag, lim, 113))) break;
+          if (j == 0 && !(ok = mbar_wait(smem_u32(&sm.o_empty[0]), (ti & 1) ^ 1, abort_flag, lim, 114))) break;
+          tc_fence_after();
+          issue_pv(0, st, j == 0);
+          // S_0 of tile j+1
+          if (more) {
+            if (!(ok = mbar_wait(smem_u32(&sm.k_full[st1]), ph1, abort_flag, lim, 115))) break;
+            tc_fence_after();
+            issue_s(0, st1);
+          }
+          // O_1 += P_1 V_j
+          if (!(ok = mbar_wait(smem_u32(&sm.p_full[1]), pf_cnt[1] & 1, abort_flag, lim, 116))) break;
+          ++pf_cnt[1];
+          if (j == 0 && !(ok = mbar_wait(smem_u32(&sm.o_empty[1]), (ti & 1) ^ 1, abort_flag, lim, 117))) break;
+          tc_fence_after();
+          issue_pv(1, st, j == 0);
+          mma_commit(smem_u32(&sm.v_empty[st]));
+          if (more) {
+            issue_s(1, st1);
+            mma_commit(smem_u32(&sm.k_empty[st1]));
+            if (j + 1 == nkv - 1) mma_commit(smem_u32(&sm.q_empty));
+          }
+        }
+        kv_cnt += nkv;
+      }
+      mma_commit(smem_u32(&sm.drain));
+      mbar_wait(smem_u32(&sm.drain), 0, abort_flag, ok ? lim : (1 << 22), 118);
+    }
+  } else if (warp >= 4) {
+    // ============================================================ softmax + epilogue (head h)
+    const int h = (warp - 4) >> 2;
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const uint32_t colS = h * BN, colO = kColO + h * D;
+    const int hq = it.hq0 + h;
+    uint32_t s_cnt = 0, pv_base = 0;
+    bool ok = true;
+    for (int ti = 0; ti < 2 && ok; ++ti) {
+      int qc, qi;
+      tile_of(p, it1, ti, qc, qi);
+      const int q_valid = min(BM, p.c - qi * BM);
+      const int nkv = n_kv_tiles(sch, qc, qi);
+      KvIter kv;
+      kv.init(sch, qc, qi);
+      float m = -CUDART_INF_F, l = 0.f;
+      for (int j = 0; j < nkv; ++j) {
+        int kc = 0, kt = 0;
+        kv.next(kc, kt);
+        const int kv_valid = min(BN, p.c - kt * BN);
+        const bool diag = p.causal && kc == qc && kt == qi;
+        if (!(ok = mbar_wait(smem_u32(&sm.s_full[h]), s_cnt & 1, abort_flag, lim, 120 + h))) break;
+        ++s_cnt;
+        tc_fence_after();
+        uint32_t sr[BN];
+#pragma unroll
+        for (int c4 = 0; c4 < BN / 32; ++c4)
+          tmem_ld32(t_lane + colS + 32 * c4, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * c4]));
+        tmem_wait_ld();
+        const int col_lim = diag ? min(kv_valid, row + 1) : kv_valid;
+        float mx = -CUDART_INF_F;
+#pragma unroll
+        for (int i = 0; i < BN; ++i) {
+          float x = __uint_as_float(sr[i]);
+          if (i >= col_lim) x = -CUDART_INF_F;
+          sr[i] = __float_as_uint(x);
+          mx = fmaxf(mx, x);
+        }
+        const float m_tile = mx * p.scale_log2;
+        const bool need = (j == 0) || (m_tile > m + 8.f);
+        const float m_use = need ? fmaxf(m, m_tile) : m;
+        const float m_ref = (m_use == -CUDART_INF_F) ? 0.f : m_use;
+        const float alpha = (j == 0) ? 0.f : exp2f(m - m_ref);
+        float rs = 0.f;
+#pragma unroll
+        for (int i = 0; i < BN; i += 2) {
+          const float p0 = exp2f(fmaf(__uint_as_float(sr[i]), p.scale_log2, -m_ref));
+          const float p1 = exp2f(fmaf(__uint_as_float(sr[i + 1]), p.scale_log2, -m_ref));
+          rs += p0 + p1;
+          sr[i >> 1] = f2_bf16x2(p0, p1);
+        }
+        l = (j == 0) ? rs : l * alpha + rs;
+        if (j > 0 && __any_sync(0xffffffffu, need && alpha != 1.f)) {
+          // O_h must hold P_{j-1} V_{j-1} before it is rescaled
+          if (!(ok = mbar_wait(smem_u32(&sm.pv_done[h]), (pv_base + j - 1) & 1, abort_flag, lim, 124 + h))) break;
+          tc_fence_after();
+          const float a = need ? alpha : 1.f;
+#pragma unroll
+          for (int c4 = 0; c4 < D / 32; ++c4) {
+            uint32_t orr[32];
+            tmem_ld32(t_lane + colO + 32 * c4, orr);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * a);
+            tmem_st32(t_lane + colO + 32 * c4, orr);
+          }
+        }
+        m = m_use;
+        // P_h into the first 64 columns of S_h
+        tmem_st32(t_lane + colS, *reinterpret_cast<const uint32_t(*)[32]>(&sr[0]));
+        tmem_st32(t_lane + colS + 32, *reinterpret_cast<const uint32_t(*)[32]>(&sr[32]));
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(smem_u32(&sm.p_full[h]));
+      }
+      if (!ok) break;
+      // ---------------------------------------------------------- epilogue
+      if (!(ok = mbar_wait(smem_u32(&sm.pv_done[h]), (pv_base + nkv - 1) & 1, abort_flag, lim, 126 + h))) break;
+      pv_base += nkv;
+      tc_fence_after();
+      const float inv_l = l > 0.f ? 1.f / l : 0.f;
+      const bool row_ok = row < q_valid;
+      const int64_t trow = token_row(p, it.b, qc, qi * BM + row);
+      __nv_bfloat16* orow = p.o + (trow * p.Hq + hq) * D;
+#pragma unroll
+      for (int c4 = 0; c4 < D / 32; ++c4) {
+        uint32_t orr[32];
+        tmem_ld32(t_lane + colO + 32 * c4, orr);
+        tmem_wait_ld();
+        if (row_ok) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 8) {
+            uint4 pk;
+            pk.x = f2_bf16x2(__uint_as_float(orr[i]) * inv_l, __uint_as_float(orr[i + 1]) * inv_l);
+            pk.y = f2_bf16x2(__uint_as_float(orr[i + 2]) * inv_l, __uint_as_float(orr[i + 3]) * inv_l);
+            pk.z = f2_bf16x2(__uint_as_float(orr[i + 4]) * inv_l, __uint_as_float(orr[i + 5]) * inv_l);
+            pk.w = f2_bf16x2(__uint_as_float(orr[i + 6]) * inv_l, __uint_as_float(orr[i + 7]) * inv_l);
+            *reinterpret_cast<uint4*>(orow + 32 * c4 + i) = pk;
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(smem_u32(&sm.o_empty[h]));
+      if (row_ok) p.lse[trow * p.Hq + hq] = l > 0.f ? (m + log2f(l)) * kLn2 : -CUDART_INF_F;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
 // Per-rank tile classification with the kernel's own iterator (for tests).
 __global__ void schedule_counts_kernel(Sched s, unsigned long long* counts) {
   const int n_tiles = 2 * s.N * s.nt;  // query tiles of the whole sequence
@@ -487,7 +815,7 @@ ra_status make_map(CUtensorMap* map, const void* base, int D, int H, int64_t row
 }
 
 template <int D>
-ra_status launch_bf16(const void* q, const void* k, const void* v, const Params& prm, int64_t items,
+ra_status launch_bf16(const void* q, const void* k, const void* v, const Params& prm, int variant,
                       cudaStream_t stream) {
   CUtensorMap mq, mk, mv;
   const int64_t rows = static_cast<int64_t>(prm.B) * prm.S;
@@ -495,10 +823,19 @@ ra_status launch_bf16(const void* q, const void* k, const void* v, const Params&
   if ((st = make_map(&mq, q, D, prm.Hq, rows)) != RA_OK) return st;
   if ((st = make_map(&mk, k, D, prm.Hkv, rows)) != RA_OK) return st;
   if ((st = make_map(&mv, v, D, prm.Hkv, rows)) != RA_OK) return st;
+  const int64_t tiles = static_cast<int64_t>(prm.B) * prm.Hq * prm.N * prm.nt;  // mirrored tile pairs x heads
+  if (variant == 2) {
+    const size_t smem = sizeof(Smem2<D>) + 1024;
+    RA_CUDA_TRY(cudaFuncSetAttribute(ring_attn_bf16_pair_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(smem)));
+    ring_attn_bf16_pair_kernel<D><<<static_cast<unsigned>(tiles / 2), kThreads2, smem, stream>>>(mq, mk, mv, prm);
+    RA_LAUNCH_CHECK("ring_attn_bf16_pair_kernel");
+    return RA_OK;
+  }
   const size_t smem = sizeof(Smem<D>) + 1024;
   RA_CUDA_TRY(cudaFuncSetAttribute(ring_attn_bf16_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    static_cast<int>(smem)));
-  ring_attn_bf16_kernel<D><<<static_cast<unsigned>(items), kThreads, smem, stream>>>(mq, mk, mv, prm);
+  ring_attn_bf16_kernel<D><<<static_cast<unsigned>(tiles), kThreads, smem, stream>>>(mq, mk, mv, prm);
   RA_LAUNCH_CHECK("ring_attn_bf16_kernel");
   return RA_OK;
 }
@@ -522,10 +859,12 @@ static long long wait_limit() {
 }
 }  // namespace ra
 
-extern "C" ra_status ra_ring_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int32_t B,
-                                      int32_t Hq, int32_t Hkv, int32_t S, int32_t d, ra_dtype dt, int32_t causal,
-                                      int32_t n_ranks, float scale, ra_layout layout, ra_stream stream) {
+extern "C" ra_status ra_ring_attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse,
+                                         int32_t B, int32_t Hq, int32_t Hkv, int32_t S, int32_t d, ra_dtype dt,
+                                         int32_t causal, int32_t n_ranks, float scale, ra_layout layout,
+                                         int32_t variant, ra_stream stream) {
   ra::clear_error();
+  RA_REQUIRE(variant >= 0 && variant <= 2, "variant must be 0, 1 or 2");
   RA_REQUIRE(B >= 1 && Hq >= 1 && Hkv >= 1 && S >= 1, "B, Hq, Hkv, S must be >= 1");
   RA_REQUIRE(Hq % Hkv == 0, "Hq (%d) must be a multiple of Hkv (%d)", Hq, Hkv);
   RA_REQUIRE(n_ranks >= 1, "n_ranks must be >= 1 (got %d)", n_ranks);
@@ -551,8 +890,16 @@ extern "C" ra_status ra_ring_attn_fwd(const void* q, const void* k, const void* 
   prm.wait_limit = ra::wait_limit();
   const int64_t items = static_cast<int64_t>(B) * Hkv * n_ranks * prm.nt * prm.group;
   RA_REQUIRE(items < (int64_t(1) << 31), "too many work items");
-  if (d == 128) return launch_bf16<128>(q, k, v, prm, items, stream);
-  return launch_bf16<64>(q, k, v, prm, items, stream);
+  if (variant == 0) variant = (prm.group % 2 == 0) ? 2 : 1;
+  RA_REQUIRE(variant == 1 || prm.group % 2 == 0, "the two-head variant needs an even Hq/Hkv");
+  if (d == 128) return launch_bf16<128>(q, k, v, prm, variant, stream);
+  return launch_bf16<64>(q, k, v, prm, variant, stream);
+}
+
+extern "C" ra_status ra_ring_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int32_t B,
+                                      int32_t Hq, int32_t Hkv, int32_t S, int32_t d, ra_dtype dt, int32_t causal,
+                                      int32_t n_ranks, float scale, ra_layout layout, ra_stream stream) {
+  return ra_ring_attn_fwd_ex(q, k, v, o, lse, B, Hq, Hkv, S, d, dt, causal, n_ranks, scale, layout, 0, stream);
 }
 
 extern "C" ra_status ra_ring_schedule_counts(int32_t S, int32_t n_ranks, int32_t causal, int64_t* counts,

@@ -30,6 +30,8 @@ SIGNATURES = {
     "ra_gather_rows": [_vp, _i64, _vp, _vp, _i64, _i64, _vp],
     "ra_ring_attn_fwd": [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _c.c_int, _i32, _i32, _f32,
                          _c.c_int, _vp],
+    "ra_ring_attn_fwd_ex": [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _c.c_int, _i32, _i32, _f32,
+                            _c.c_int, _i32, _vp],
     "ra_ring_schedule_counts": [_i32, _i32, _i32, _vp, _vp],
     "ra_lse_merge": [_vp, _vp, _i32, _i64, _i32, _i32, _vp, _c.c_int, _vp, _vp],
     "ra_cp_slot_mapping": [_vp, _vp, _vp, _i32, _i32, _i64, _i32, _i32, _i32, _i32, _vp, _vp],
@@ -144,10 +146,11 @@ def gather_rows(src: torch.Tensor, idx: torch.Tensor, out: Optional[torch.Tensor
 # ---------------------------------------------------------------------- attention
 
 def ring_attn_fwd(q, k, v, causal: bool, n_ranks: int, B: int = 1, scale: Optional[float] = None,
-                  layout: str = "natural", o=None, lse=None):
+                  layout: str = "natural", o=None, lse=None, variant: int = 0):
     """Ring-order attention forward.  q [B*S, Hq, d], k/v [B*S, Hkv, d] token-major.
 
-    Returns (O [B*S, Hq, d] in q's dtype, LSE float32 [B*S, Hq])."""
+    Returns (O [B*S, Hq, d] in q's dtype, LSE float32 [B*S, Hq]).  ``variant`` picks the
+    bf16 kernel (0 automatic, 1 one head per CTA, 2 two GQA heads per CTA)."""
     _need_cuda(q, k, v, o, lse)
     rows, Hq, d = q.shape
     Hkv = k.shape[1]
@@ -158,8 +161,9 @@ def ring_attn_fwd(q, k, v, causal: bool, n_ranks: int, B: int = 1, scale: Option
         o = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((rows, Hq), dtype=torch.float32, device=q.device)
-    _check(lib().ra_ring_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, S, d, _dt(q),
-                                  1 if causal else 0, n_ranks, float(scale or 0.0), LAYOUTS[layout], _stream()))
+    _check(lib().ra_ring_attn_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, S, d, _dt(q),
+                                     1 if causal else 0, n_ranks, float(scale or 0.0), LAYOUTS[layout], variant,
+                                     _stream()))
     return o, lse
 
 

@@ -128,6 +128,17 @@ ra_status ra_ring_attn_fwd(const void* q, const void* k, const void* v, void* o,
                            ra_dtype dt, int32_t causal, int32_t n_ranks, float scale,
                            ra_layout layout, ra_stream stream);
 
+/* Same as ra_ring_attn_fwd with an explicit bf16 kernel variant:
+ * 0 = automatic (2 when Hq/Hkv is even, else 1);
+ * 1 = one query head per CTA (mirrored pair of query tiles, P via shared memory);
+ * 2 = two query heads of one GQA group per CTA sharing every K/V tile (needs an
+ *     even Hq/Hkv; P stays in tensor memory).
+ * The variant is ignored for RA_F32.  Results of 1 and 2 agree to rounding. */
+ra_status ra_ring_attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse,
+                              int32_t B, int32_t Hq, int32_t Hkv, int32_t S, int32_t d,
+                              ra_dtype dt, int32_t causal, int32_t n_ranks, float scale,
+                              ra_layout layout, int32_t variant, ra_stream stream);
+
 /* ------------------------------------------------------------------------
  * ra_ring_schedule_counts -- the (query tile, key tile) classification the
  * bf16 ring kernel uses, counted per virtual rank on the device by the same

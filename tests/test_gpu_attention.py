@@ -15,15 +15,15 @@ def ra():
     return ra_lib()
 
 
-def _run(ra, seed, B, S, Hq, Hkv, d, N, causal, dtype, layout="natural"):
+def _run(ra, seed, B, S, Hq, Hkv, d, N, causal, dtype, layout="natural", variant=0):
     q, k, v = I.prefill_inputs(seed, B, S, Hq, Hkv, d, dtype)
     dev = torch.device("cuda")
     if layout == "natural":
-        o, lse = ra.ring_attn_fwd(q.to(dev), k.to(dev), v.to(dev), causal, N, B=B)
+        o, lse = ra.ring_attn_fwd(q.to(dev), k.to(dev), v.to(dev), causal, N, B=B, variant=variant)
     else:
         perm, restore = ra.zigzag_partition([S] * B, N)
         qz, kz, vz = (ra.gather_rows(x.to(dev), perm) for x in (q, k, v))
-        oz, lz = ra.ring_attn_fwd(qz, kz, vz, causal, N, B=B, layout="zigzag")
+        oz, lz = ra.ring_attn_fwd(qz, kz, vz, causal, N, B=B, layout="zigzag", variant=variant)
         o, lse = ra.gather_rows(oz, restore), ra.gather_rows(lz, restore)
     check_status(ra)
     return q, k, v, o, lse
@@ -67,10 +67,21 @@ def test_fp32_ragged_and_gqa(ra, S, N, causal, Hq, Hkv, d):
     (2048, 4, 1, 2, 2, 64, False),
     (16, 8, 1, 2, 2, 128, True),       # chunks of 1 token
 ])
-def test_bf16_parity_small(ra, S, N, B, Hq, Hkv, d, causal):
-    q, k, v, o, lse = _run(ra, 3, B, S, Hq, Hkv, d, N, causal, torch.bfloat16)
+@pytest.mark.parametrize("variant", [1, 2])
+def test_bf16_parity_small(ra, S, N, B, Hq, Hkv, d, causal, variant):
+    if variant == 2 and (Hq // Hkv) % 2:
+        Hq = 2 * Hq                       # the two-head kernel needs an even GQA group
+    q, k, v, o, lse = _run(ra, 3, B, S, Hq, Hkv, d, N, causal, torch.bfloat16, variant=variant)
     O, L = _oracle_full(q, k, v, B, S, causal)
-    assert_parity(o, O, lse, L, torch.bfloat16, "bf16 S=%d N=%d" % (S, N))
+    assert_parity(o, O, lse, L, torch.bfloat16, "bf16 v%d S=%d N=%d" % (variant, S, N))
+
+
+def test_bf16_variants_agree(ra):
+    B, S, Hq, Hkv, d, N = 1, 2560, 8, 2, 128, 5
+    _, _, _, o1, l1 = _run(ra, 6, B, S, Hq, Hkv, d, N, True, torch.bfloat16, variant=1)
+    _, _, _, o2, l2 = _run(ra, 6, B, S, Hq, Hkv, d, N, True, torch.bfloat16, variant=2)
+    assert (o1.float() - o2.float()).abs().max().item() <= 1.6e-2
+    assert (l1 - l2).abs().max().item() <= 1e-4
 
 
 def test_bf16_zigzag_layout_is_bitwise_natural(ra):
