@@ -451,9 +451,12 @@ def main():
                     help="'all' for the benchmark line, else 'prefill', 'decode' or 'prefill,decode' "
                          "to run only those parts (profiler captures)")
     ap.add_argument("--prefill-seq", type=int, default=None, help="override S of the prefill (multiple of 2N)")
+    ap.add_argument("--decode-requests", type=int, default=None, help="override the number of decode requests")
     args = ap.parse_args()
     if args.prefill_seq:
         PREFILL["S"] = args.prefill_seq
+    if args.decode_requests:
+        DECODE["R"] = args.decode_requests
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if args.impl == "reference":

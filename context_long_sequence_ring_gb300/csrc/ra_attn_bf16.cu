@@ -144,6 +144,56 @@ __device__ __forceinline__ uint32_t f2_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// 2^x with the SFU instruction (flush-to-zero; 2^-inf = 0).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Online-softmax step of one score row held in registers (raw Q.K^T values).
+// Masks columns >= col_lim when `masked`, returns the row max of the raw
+// scores; independent partial maxima keep the dependency chains short.
+__device__ __forceinline__ float row_max_masked(uint32_t (&sr)[BN], bool masked, int col_lim) {
+  if (masked) {
+#pragma unroll
+    for (int i = 0; i < BN; ++i)
+      if (i >= col_lim) sr[i] = __float_as_uint(-CUDART_INF_F);
+  }
+  float mx[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) mx[k] = __uint_as_float(sr[k]);
+#pragma unroll
+  for (int i = 8; i < BN; i += 8)
+#pragma unroll
+    for (int k = 0; k < 8; ++k) mx[k] = fmaxf(mx[k], __uint_as_float(sr[i + k]));
+#pragma unroll
+  for (int k = 4; k > 0; k >>= 1)
+#pragma unroll
+    for (int t = 0; t < k; ++t) mx[t] = fmaxf(mx[t], mx[t + k]);
+  return mx[0];
+}
+
+// p = 2^(s*scale - m_ref) for the row, packed to bf16 pairs into sr[0..BN/2);
+// returns the fp32 row sum.
+__device__ __forceinline__ float row_exp_pack(uint32_t (&sr)[BN], float scale_log2, float m_ref) {
+  float acc[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) acc[k] = 0.f;
+#pragma unroll
+  for (int i = 0; i < BN; i += 2) {
+    const float p0 = ex2(fmaf(__uint_as_float(sr[i]), scale_log2, -m_ref));
+    const float p1 = ex2(fmaf(__uint_as_float(sr[i + 1]), scale_log2, -m_ref));
+    acc[(i >> 1) & 7] += p0 + p1;
+    sr[i >> 1] = f2_bf16x2(p0, p1);
+  }
+#pragma unroll
+  for (int k = 4; k > 0; k >>= 1)
+#pragma unroll
+    for (int t = 0; t < k; ++t) acc[t] += acc[t + k];
+  return acc[0];
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     ring_attn_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -335,27 +385,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++s_cnt;
         // mask (raw scores) and row max
         const int col_lim = diag ? min(kv_valid, row + 1) : kv_valid;
-        float mx = -CUDART_INF_F;
-#pragma unroll
-        for (int i = 0; i < BN; ++i) {
-          float x = __uint_as_float(sr[i]);
-          if (i >= col_lim) x = -CUDART_INF_F;
-          sr[i] = __float_as_uint(x);
-          mx = fmaxf(mx, x);
-        }
-        const float m_tile = mx * p.scale_log2;
+        const bool masked = diag || kv_valid < BN;
+        const float m_tile = row_max_masked(sr, masked, col_lim) * p.scale_log2;
         const bool need = (j == 0) || (m_tile > m + 8.f);
         const float m_use = need ? fmaxf(m, m_tile) : m;
         const float m_ref = (m_use == -CUDART_INF_F) ? 0.f : m_use;
-        const float alpha = (j == 0) ? 0.f : exp2f(m - m_ref);
-        float rs = 0.f;
-#pragma unroll
-        for (int i = 0; i < BN; i += 2) {
-          const float p0 = exp2f(fmaf(__uint_as_float(sr[i]), p.scale_log2, -m_ref));
-          const float p1 = exp2f(fmaf(__uint_as_float(sr[i + 1]), p.scale_log2, -m_ref));
-          rs += p0 + p1;
-          sr[i >> 1] = f2_bf16x2(p0, p1);   // packed P in the first BN/2 words
-        }
+        const float alpha = (j == 0) ? 0.f : ex2(m - m_ref);
+        const float rs = row_exp_pack(sr, p.scale_log2, m_ref);   // packed P in sr[0..BN/2)
         l = (j == 0) ? rs : l * alpha + rs;
         if (j > 0) {
           // P_{j-1} V_{j-1} must be complete: P buffer reuse and O rescale
@@ -674,27 +710,13 @@ __global__ void __launch_bounds__(kThreads2, 1)
           tmem_ld32(t_lane + colS + 32 * c4, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * c4]));
         tmem_wait_ld();
         const int col_lim = diag ? min(kv_valid, row + 1) : kv_valid;
-        float mx = -CUDART_INF_F;
-#pragma unroll
-        for (int i = 0; i < BN; ++i) {
-          float x = __uint_as_float(sr[i]);
-          if (i >= col_lim) x = -CUDART_INF_F;
-          sr[i] = __float_as_uint(x);
-          mx = fmaxf(mx, x);
-        }
-        const float m_tile = mx * p.scale_log2;
+        const bool masked = diag || kv_valid < BN;
+        const float m_tile = row_max_masked(sr, masked, col_lim) * p.scale_log2;
         const bool need = (j == 0) || (m_tile > m + 8.f);
         const float m_use = need ? fmaxf(m, m_tile) : m;
         const float m_ref = (m_use == -CUDART_INF_F) ? 0.f : m_use;
-        const float alpha = (j == 0) ? 0.f : exp2f(m - m_ref);
-        float rs = 0.f;
-#pragma unroll
-        for (int i = 0; i < BN; i += 2) {
-          const float p0 = exp2f(fmaf(__uint_as_float(sr[i]), p.scale_log2, -m_ref));
-          const float p1 = exp2f(fmaf(__uint_as_float(sr[i + 1]), p.scale_log2, -m_ref));
-          rs += p0 + p1;
-          sr[i >> 1] = f2_bf16x2(p0, p1);
-        }
+        const float alpha = (j == 0) ? 0.f : ex2(m - m_ref);
+        const float rs = row_exp_pack(sr, p.scale_log2, m_ref);   // packed P in sr[0..BN/2)
         l = (j == 0) ? rs : l * alpha + rs;
         if (j > 0 && __any_sync(0xffffffffu, need && alpha != 1.f)) {
           // O_h must hold P_{j-1} V_{j-1} before it is rescaled
