@@ -17,6 +17,8 @@
 // the kernel is bound by HBM.  Softmax runs in fp32 in the log2 domain.
 #include <math_constants.h>
 
+#include <mutex>
+
 #include "ra_common.cuh"
 
 RA_DEFINE_ERROR_FETCH(fetch_error_decode)
@@ -406,4 +408,74 @@ extern "C" ra_status ra_cp_decode(const void* q, const void* k_cache, const void
   RA_LAUNCH_CHECK("cp_decode_kernel");
   return launch_merge(prm.o_parts, prm.lse_parts, static_cast<int>(P), static_cast<int64_t>(R) * Hq, d, o,
                       out_dt, lse, stream);
+}
+
+// ===========================================================================
+// Allocation-free decode.
+//
+// Some callers cannot call cudaMalloc on the path where decode runs: an
+// inference runtime that reserves all device memory at start-up and forbids
+// allocation afterwards, code running under an allocator that cannot hand out
+// raw scratch, or a host process that must keep its device footprint fixed.
+// ra_cp_decode_noalloc gives them the same decode with the fp32 partials kept
+// in a fixed scratch array that lives in this library's device memory instead
+// of a caller-provided workspace.  Every GPU that loads the library holds the
+// array (kNoAllocScratchBytes) until the process exits.
+//
+// The array's name is a host-side stand-in in host code, not a device
+// address; its device address is looked up once per device (with that device
+// current) by cudaGetSymbolAddress, the first time the entry point runs on
+// that device, and then reused.
+//
+// All calls share the array and it keeps the last call's contents.  Nothing in
+// it has to start at zero: each call writes the LSE of every partial before the
+// merge reads it, and the merge reads a partial's O only when that LSE is
+// finite, i.e. when the same call wrote that O.  Calls whose work overlaps on
+// the GPU (for example on two streams at once) race on the array.
+// ===========================================================================
+constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;  // 32 MiB
+static __device__ __align__(256) unsigned char g_decode_scratch[kNoAllocScratchBytes];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mutex;
+void* g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of g_decode_scratch on the current device (looked up once).
+ra_status scratch_address(void** out) {
+  int dev = 0;
+  RA_CUDA_TRY(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= kMaxDevices) return ra::fail(RA_ERR_UNSUPPORTED, "device index %d out of range", dev);
+  std::lock_guard<std::mutex> lock(g_scratch_mutex);
+  if (g_scratch_ptr[dev] == nullptr) {
+    void* ptr = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&ptr, g_decode_scratch);
+    if (e != cudaSuccess) return ra::cuda_status(e, "cudaGetSymbolAddress(decode scratch)");
+    g_scratch_ptr[dev] = ptr;
+  }
+  *out = g_scratch_ptr[dev];
+  return RA_OK;
+}
+}  // namespace
+
+extern "C" ra_status ra_cp_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                          const int32_t* block_table, const int32_t* ctx_lens, int32_t R,
+                                          int32_t Hq, int32_t Hkv, int32_t d, int32_t block_size,
+                                          int32_t interleave, int32_t pcp, int32_t dcp, int32_t max_vblocks,
+                                          int64_t num_blocks, float scale, int32_t split_blocks, void* o,
+                                          ra_dtype out_dt, float* lse, ra_stream stream) {
+  ra::clear_error();
+  size_t need = 0;
+  ra_status st = ra_cp_decode_workspace_size(R, Hq, d, max_vblocks, pcp, dcp, split_blocks, &need);
+  if (st != RA_OK) return st;
+  if (need > kNoAllocScratchBytes)
+    return ra::fail(RA_ERR_INVALID_ARG,
+                    "this decode needs %zu bytes of scratch, but the allocation-free entry point holds at most "
+                    "%zu bytes; raise split_blocks or call ra_cp_decode with a workspace",
+                    need, kNoAllocScratchBytes);
+  void* scratch = nullptr;
+  if ((st = scratch_address(&scratch)) != RA_OK) return st;
+  return ra_cp_decode(q, k_cache, v_cache, block_table, ctx_lens, R, Hq, Hkv, d, block_size, interleave, pcp,
+                      dcp, max_vblocks, num_blocks, scale, split_blocks, o, out_dt, lse, scratch,
+                      kNoAllocScratchBytes, stream);
 }

@@ -39,6 +39,8 @@ SIGNATURES = {
     "ra_cp_decode_workspace_size": [_i32, _i32, _i32, _i32, _i32, _i32, _i32, _c.POINTER(_sz)],
     "ra_cp_decode": [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i64, _f32,
                      _i32, _vp, _c.c_int, _vp, _vp, _sz, _vp],
+    "ra_cp_decode_noalloc": [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i64,
+                             _f32, _i32, _vp, _c.c_int, _vp, _vp],
     "ra_selftest_wait_timeout": [_i64, _vp],
     "ra_synth_fill": [_u64, _i64, _vp, _i32, _vp, _vp],
 }
@@ -234,6 +236,26 @@ def cp_decode(q, k_cache, v_cache, block_table, ctx_lens, interleave: int, pcp: 
                               d, bs, interleave, pcp, dcp, max_vb, NB, float(scale or 0.0), split_blocks, _ptr(o),
                               RA_BF16 if o.dtype == torch.bfloat16 else RA_F32, _ptr(lse), _ptr(workspace),
                               workspace.numel() * workspace.element_size(), _stream()))
+    return o, lse
+
+
+def cp_decode_noalloc(q, k_cache, v_cache, block_table, ctx_lens, interleave: int, pcp: int, dcp: int,
+                      split_blocks: int = 8, scale: Optional[float] = None, out_dtype=torch.bfloat16, o=None,
+                      lse=None):
+    """cp_decode without a workspace, for callers that cannot allocate device memory on the decode
+    path: the partials live in a fixed 32 MiB scratch array inside the library (shared by all
+    calls; calls that overlap on the GPU race).  Outputs o/lse may be passed in preallocated."""
+    _need_cuda(q, k_cache, v_cache, block_table, ctx_lens, o, lse)
+    R, Hq, d = q.shape
+    W, NB, Hkv, bs, _ = k_cache.shape
+    if o is None:
+        o = torch.empty((R, Hq, d), dtype=out_dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty((R, Hq), dtype=torch.float32, device=q.device)
+    _check(lib().ra_cp_decode_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(ctx_lens), R,
+                                      Hq, Hkv, d, bs, interleave, pcp, dcp, block_table.shape[1], NB,
+                                      float(scale or 0.0), split_blocks, _ptr(o),
+                                      RA_BF16 if o.dtype == torch.bfloat16 else RA_F32, _ptr(lse), _stream()))
     return o, lse
 
 

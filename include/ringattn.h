@@ -240,6 +240,36 @@ ra_status ra_cp_decode(const void* q, const void* k_cache, const void* v_cache,
                        ra_stream stream);
 
 /* ------------------------------------------------------------------------
+ * ra_cp_decode_noalloc -- ra_cp_decode for callers that cannot allocate
+ * device memory on the decode path (a runtime that reserves all device memory
+ * at start-up and forbids allocation afterwards, an allocator that cannot
+ * hand out raw scratch, a process whose device footprint must stay fixed).
+ * The pages have no counterpart of this entry point; it only changes where
+ * the scratch lives.
+ *
+ * Same arguments and results as ra_cp_decode, without workspace/ws_bytes:
+ * the fp32 partials go to a fixed 32 MiB scratch array inside the library's
+ * device memory, which every GPU that loads the library holds until exit.
+ * Nothing is allocated and no allocating routine is called.
+ * - A decode whose partials need more than 32 MiB
+ *   (ra_cp_decode_workspace_size) is rejected with RA_ERR_INVALID_ARG; a
+ *   larger split_blocks makes it smaller.
+ * - The first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress, with that device current) and caches it; make that
+ *   first call before any stream capture.
+ * - All calls share the array and it keeps the last call's contents.  Nothing
+ *   in it needs to start at zero (every partial's LSE is written before it is
+ *   read, and a partial's O is read only if the same call wrote it).  Calls
+ *   whose work overlaps on the GPU (e.g. on two streams) race on the array.
+ * ---------------------------------------------------------------------- */
+ra_status ra_cp_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                               const int32_t* block_table, const int32_t* ctx_lens, int32_t R,
+                               int32_t Hq, int32_t Hkv, int32_t d, int32_t block_size,
+                               int32_t interleave, int32_t pcp, int32_t dcp, int32_t max_vblocks,
+                               int64_t num_blocks, float scale, int32_t split_blocks, void* o,
+                               ra_dtype out_dt, float* lse, ra_stream stream);
+
+/* ------------------------------------------------------------------------
  * Self-test of the bounded-wait machinery: launches one CTA that waits on an
  * mbarrier nobody arrives at, for at most `limit_cycles` SM clock cycles,
  * then records RA_ERR_TIMEOUT in the device error word and returns.  The
