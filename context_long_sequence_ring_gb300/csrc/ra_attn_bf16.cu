@@ -151,47 +151,128 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// Online-softmax step of one score row held in registers (raw Q.K^T values).
-// Masks columns >= col_lim when `masked`, returns the row max of the raw
-// scores; independent partial maxima keep the dependency chains short.
-__device__ __forceinline__ float row_max_masked(uint32_t (&sr)[BN], bool masked, int col_lim) {
-  if (masked) {
-#pragma unroll
-    for (int i = 0; i < BN; ++i)
-      if (i >= col_lim) sr[i] = __float_as_uint(-CUDART_INF_F);
-  }
-  float mx[8];
-#pragma unroll
-  for (int k = 0; k < 8; ++k) mx[k] = __uint_as_float(sr[k]);
-#pragma unroll
-  for (int i = 8; i < BN; i += 8)
-#pragma unroll
-    for (int k = 0; k < 8; ++k) mx[k] = fmaxf(mx[k], __uint_as_float(sr[i + k]));
-#pragma unroll
-  for (int k = 4; k > 0; k >>= 1)
-#pragma unroll
-    for (int t = 0; t < k; ++t) mx[t] = fmaxf(mx[t], mx[t + k]);
-  return mx[0];
+// ------------------------------------------------------------------ softmax of one row
+__device__ __forceinline__ uint64_t f2pack(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2unpack(uint64_t r, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
 }
 
-// p = 2^(s*scale - m_ref) for the row, packed to bf16 pairs into sr[0..BN/2);
-// returns the fp32 row sum.
-__device__ __forceinline__ float row_exp_pack(uint32_t (&sr)[BN], float scale_log2, float m_ref) {
-  float acc[8];
+// Columns [c0, c0+32) of a score row: mask (when asked) and return the max.
+__device__ __forceinline__ float chunk_mask_max(uint32_t (&x)[32], int c0, bool masked, int col_lim) {
+  if (masked) {
 #pragma unroll
-  for (int k = 0; k < 8; ++k) acc[k] = 0.f;
-#pragma unroll
-  for (int i = 0; i < BN; i += 2) {
-    const float p0 = ex2(fmaf(__uint_as_float(sr[i]), scale_log2, -m_ref));
-    const float p1 = ex2(fmaf(__uint_as_float(sr[i + 1]), scale_log2, -m_ref));
-    acc[(i >> 1) & 7] += p0 + p1;
-    sr[i >> 1] = f2_bf16x2(p0, p1);
+    for (int i = 0; i < 32; ++i)
+      if (c0 + i >= col_lim) x[i] = __float_as_uint(-CUDART_INF_F);
   }
+  float mx[4];
 #pragma unroll
-  for (int k = 4; k > 0; k >>= 1)
+  for (int k = 0; k < 4; ++k) mx[k] = __uint_as_float(x[k]);
 #pragma unroll
-    for (int t = 0; t < k; ++t) acc[t] += acc[t + k];
-  return acc[0];
+  for (int i = 4; i < 32; i += 8)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) mx[k] = fmax3(mx[k], __uint_as_float(x[i + k]), __uint_as_float(x[i + 4 + k]));
+  return fmax3(fmax3(mx[0], mx[1], mx[2]), mx[3], mx[3]);
+}
+
+// p = 2^(s*scale - m_ref) for 32 columns, packed to bf16 pairs into pk[0..16); adds the
+// fp32 sums into two packed accumulators.
+__device__ __forceinline__ void chunk_exp_pack(const uint32_t (&x)[32], uint64_t sc2, uint64_t negm2,
+                                               uint64_t& acc0, uint64_t& acc1, uint32_t* pk) {
+#pragma unroll
+  for (int i = 0; i < 32; i += 2) {
+    float t0, t1;
+    f2unpack(ffma2(f2pack(__uint_as_float(x[i]), __uint_as_float(x[i + 1])), sc2, negm2), t0, t1);
+    const float p0 = ex2(t0), p1 = ex2(t1);
+    if ((i >> 1) & 1) acc1 = fadd2(acc1, f2pack(p0, p1)); else acc0 = fadd2(acc0, f2pack(p0, p1));
+    pk[i >> 1] = f2_bf16x2(p0, p1);
+  }
+}
+
+// One online-softmax step for the score row at tensor-memory address s_addr
+// (BN fp32 columns, raw Q.K^T): fills pk with P in bf16 pairs and updates the
+// running max m (log2 units) and sum l.  Returns the factor O must be scaled by
+// (1 when unchanged).
+//
+// After the first K/V tile the row is read once, 32 columns at a time, with the
+// running max as reference: the exps start before the whole row is seen.  If
+// any row of the warp finds a score above max + 8 (log2), the warp falls back
+// to two passes (max, then exps) and the rows that grew move their reference.
+// The stale reference is exact because l and O always share it; 2^8 bounds P.
+__device__ __forceinline__ float softmax_row(uint32_t s_addr, int j, bool masked, int col_lim, float scale,
+                                             float& m, float& l, uint32_t (&pk)[BN / 2]) {
+  const uint64_t sc2 = f2pack(scale, scale);
+  if (j > 0) {
+    const float thr = (m + 8.f) / scale;   // raw-score threshold of a rescale
+    const uint64_t negm2 = f2pack(-m, -m);
+    uint64_t acc0 = f2pack(0.f, 0.f), acc1 = acc0;
+    bool grow = false;
+#pragma unroll
+    for (int c = 0; c < BN / 32; ++c) {
+      uint32_t x[32];
+      tmem_ld32(s_addr + 32 * c, x);
+      tmem_wait_ld();
+      const float cm = chunk_mask_max(x, 32 * c, masked, col_lim);
+      if (__any_sync(0xffffffffu, cm > thr)) { grow = true; break; }
+      chunk_exp_pack(x, sc2, negm2, acc0, acc1, &pk[16 * c]);
+    }
+    if (!grow) {
+      float a0, a1, b0, b1;
+      f2unpack(acc0, a0, a1);
+      f2unpack(acc1, b0, b1);
+      l += (a0 + a1) + (b0 + b1);
+      return 1.f;
+    }
+  }
+  // two passes: the row max, then the exps against the (possibly new) reference
+  float mx = -CUDART_INF_F;
+#pragma unroll
+  for (int c = 0; c < BN / 32; ++c) {
+    uint32_t x[32];
+    tmem_ld32(s_addr + 32 * c, x);
+    tmem_wait_ld();
+    mx = fmaxf(mx, chunk_mask_max(x, 32 * c, masked, col_lim));
+  }
+  const float m_tile = mx * scale;
+  const bool need = (j == 0) || (m_tile > m + 8.f);
+  const float m_use = need ? fmaxf(m, m_tile) : m;
+  const float m_ref = (m_use == -CUDART_INF_F) ? 0.f : m_use;
+  const float alpha = (j == 0) ? 0.f : ex2(m - m_ref);
+  const uint64_t negm2 = f2pack(-m_ref, -m_ref);
+  uint64_t acc0 = f2pack(0.f, 0.f), acc1 = acc0;
+#pragma unroll
+  for (int c = 0; c < BN / 32; ++c) {
+    uint32_t x[32];
+    tmem_ld32(s_addr + 32 * c, x);
+    tmem_wait_ld();
+    chunk_mask_max(x, 32 * c, masked, col_lim);
+    chunk_exp_pack(x, sc2, negm2, acc0, acc1, &pk[16 * c]);
+  }
+  float a0, a1, b0, b1;
+  f2unpack(acc0, a0, a1);
+  f2unpack(acc1, b0, b1);
+  const float rs = (a0 + a1) + (b0 + b1);
+  l = (j == 0) ? rs : l * alpha + rs;
+  m = m_use;
+  return (j == 0) ? 1.f : alpha;
 }
 
 template <int D>
@@ -375,51 +456,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t sph = (s_cnt >> 1) & 1;
         if (!(ok = mbar_wait(smem_u32(&sm.s_full[sb]), sph, abort_flag, lim, 20))) break;
         tc_fence_after();
-        uint32_t sr[BN];
-#pragma unroll
-        for (int c4 = 0; c4 < BN / 32; ++c4)
-          tmem_ld32(t_lane + kColS0 + sb * BN + 32 * c4, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * c4]));
-        tmem_wait_ld();
+        const int col_lim = diag ? min(kv_valid, row + 1) : kv_valid;
+        const bool masked = diag || kv_valid < BN;
+        uint32_t pk[BN / 2];
+        const float alpha = softmax_row(t_lane + kColS0 + sb * BN, j, masked, col_lim, p.scale_log2, m, l, pk);
         tc_fence_before();
         mbar_arrive(smem_u32(&sm.s_empty[sb]));
         ++s_cnt;
-        // mask (raw scores) and row max
-        const int col_lim = diag ? min(kv_valid, row + 1) : kv_valid;
-        const bool masked = diag || kv_valid < BN;
-        const float m_tile = row_max_masked(sr, masked, col_lim) * p.scale_log2;
-        const bool need = (j == 0) || (m_tile > m + 8.f);
-        const float m_use = need ? fmaxf(m, m_tile) : m;
-        const float m_ref = (m_use == -CUDART_INF_F) ? 0.f : m_use;
-        const float alpha = (j == 0) ? 0.f : ex2(m - m_ref);
-        const float rs = row_exp_pack(sr, p.scale_log2, m_ref);   // packed P in sr[0..BN/2)
-        l = (j == 0) ? rs : l * alpha + rs;
         if (j > 0) {
           // P_{j-1} V_{j-1} must be complete: P buffer reuse and O rescale
           if (!(ok = mbar_wait(smem_u32(&sm.pv_done), pv_cnt & 1, abort_flag, lim, 21))) break;
           ++pv_cnt;
           tc_fence_after();
-          if (__any_sync(0xffffffffu, need && alpha != 1.f)) {
-            const float a = need ? alpha : 1.f;
+          if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
             for (int c4 = 0; c4 < D / 32; ++c4) {
               uint32_t orr[32];
               tmem_ld32(t_lane + kColO + 32 * c4, orr);
               tmem_wait_ld();
 #pragma unroll
-              for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * a);
+              for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
               tmem_st32(t_lane + kColO + 32 * c4, orr);
             }
             tmem_wait_st();
           }
         }
-        m = m_use;
         // P (bf16, 128-byte swizzle, K-major) into shared memory
 #pragma unroll
         for (int ch = 0; ch < BN / 8; ++ch) {
           const int slab = ch >> 3, c16 = ch & 7;
           const uint32_t addr = p_base + slab * (BM * 128) + row * 128 + ((c16 ^ (row & 7)) << 4);
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(sr[4 * ch]),
-                       "r"(sr[4 * ch + 1]), "r"(sr[4 * ch + 2]), "r"(sr[4 * ch + 3])
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[4 * ch]),
+                       "r"(pk[4 * ch + 1]), "r"(pk[4 * ch + 2]), "r"(pk[4 * ch + 3])
                        : "memory");
         }
         fence_proxy_async_smem();
@@ -704,39 +772,27 @@ __global__ void __launch_bounds__(kThreads2, 1)
         if (!(ok = mbar_wait(smem_u32(&sm.s_full[h]), s_cnt & 1, abort_flag, lim, 120 + h))) break;
         ++s_cnt;
         tc_fence_after();
-        uint32_t sr[BN];
-#pragma unroll
-        for (int c4 = 0; c4 < BN / 32; ++c4)
-          tmem_ld32(t_lane + colS + 32 * c4, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * c4]));
-        tmem_wait_ld();
         const int col_lim = diag ? min(kv_valid, row + 1) : kv_valid;
         const bool masked = diag || kv_valid < BN;
-        const float m_tile = row_max_masked(sr, masked, col_lim) * p.scale_log2;
-        const bool need = (j == 0) || (m_tile > m + 8.f);
-        const float m_use = need ? fmaxf(m, m_tile) : m;
-        const float m_ref = (m_use == -CUDART_INF_F) ? 0.f : m_use;
-        const float alpha = (j == 0) ? 0.f : ex2(m - m_ref);
-        const float rs = row_exp_pack(sr, p.scale_log2, m_ref);   // packed P in sr[0..BN/2)
-        l = (j == 0) ? rs : l * alpha + rs;
-        if (j > 0 && __any_sync(0xffffffffu, need && alpha != 1.f)) {
+        uint32_t pk[BN / 2];
+        const float alpha = softmax_row(t_lane + colS, j, masked, col_lim, p.scale_log2, m, l, pk);
+        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
           // O_h must hold P_{j-1} V_{j-1} before it is rescaled
           if (!(ok = mbar_wait(smem_u32(&sm.pv_done[h]), (pv_base + j - 1) & 1, abort_flag, lim, 124 + h))) break;
           tc_fence_after();
-          const float a = need ? alpha : 1.f;
 #pragma unroll
           for (int c4 = 0; c4 < D / 32; ++c4) {
             uint32_t orr[32];
             tmem_ld32(t_lane + colO + 32 * c4, orr);
             tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * a);
+            for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
             tmem_st32(t_lane + colO + 32 * c4, orr);
           }
         }
-        m = m_use;
         // P_h into the first 64 columns of S_h
-        tmem_st32(t_lane + colS, *reinterpret_cast<const uint32_t(*)[32]>(&sr[0]));
-        tmem_st32(t_lane + colS + 32, *reinterpret_cast<const uint32_t(*)[32]>(&sr[32]));
+        tmem_st32(t_lane + colS, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
+        tmem_st32(t_lane + colS + 32, *reinterpret_cast<const uint32_t(*)[32]>(&pk[32]));
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(smem_u32(&sm.p_full[h]));
