@@ -225,14 +225,19 @@ __device__ __forceinline__ float softmax_row(uint32_t s_addr, int j, bool masked
     const uint64_t negm2 = f2pack(-m, -m);
     uint64_t acc0 = f2pack(0.f, 0.f), acc1 = acc0;
     bool grow = false;
+    // the load of chunk c+1 is in flight while chunk c is processed
+    uint32_t xa[32], xb[32];
+    tmem_ld32(s_addr, xa);
+    tmem_wait_ld();
 #pragma unroll
     for (int c = 0; c < BN / 32; ++c) {
-      uint32_t x[32];
-      tmem_ld32(s_addr + 32 * c, x);
-      tmem_wait_ld();
+      uint32_t (&x)[32] = (c & 1) ? xb : xa;
+      uint32_t (&y)[32] = (c & 1) ? xa : xb;
+      if (c + 1 < BN / 32) tmem_ld32(s_addr + 32 * (c + 1), y);
       const float cm = chunk_mask_max(x, 32 * c, masked, col_lim);
-      if (__any_sync(0xffffffffu, cm > thr)) { grow = true; break; }
+      if (__any_sync(0xffffffffu, cm > thr)) { grow = true; tmem_wait_ld(); break; }
       chunk_exp_pack(x, sc2, negm2, acc0, acc1, &pk[16 * c]);
+      if (c + 1 < BN / 32) tmem_wait_ld();
     }
     if (!grow) {
       float a0, a1, b0, b1;
@@ -674,23 +679,24 @@ __global__ void __launch_bounds__(kThreads2, 1)
     if (lane == 0) {
       uint32_t kv_cnt = 0, pf_cnt[2] = {0, 0};
       bool ok = true;
+      // descriptors of k-step 0; a k-step adds its byte offset / 16 to the start-address field
+      const uint64_t dq[2] = {desc_sw128(smem_u32(sm.q[0]), 16, 1024), desc_sw128(smem_u32(sm.q[1]), 16, 1024)};
+      const uint64_t dk[STAGES] = {desc_sw128(smem_u32(sm.k[0]), 16, 1024), desc_sw128(smem_u32(sm.k[1]), 16, 1024)};
+      const uint64_t dv[STAGES] = {desc_sw128(smem_u32(sm.v[0]), BN * 128, 1024),
+                                   desc_sw128(smem_u32(sm.v[1]), BN * 128, 1024)};
       auto issue_s = [&](int h, int st) {
-        const uint32_t q_base = smem_u32(sm.q[h]), k_base = smem_u32(sm.k[st]);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
-          mma_bf16_ss(tmem + h * BN, desc_sw128(q_base + off, 16, 1024),
-                      desc_sw128(k_base + (kk >> 2) * (BN * 128) + (kk & 3) * 32, 16, 1024), kIdescS,
-                      kk > 0 ? 1u : 0u);
+          const uint32_t off16 = ((kk >> 2) * (BM * 128) + (kk & 3) * 32) >> 4;
+          mma_bf16_ss(tmem + h * BN, dq[h] + off16, dk[st] + off16, kIdescS, kk > 0 ? 1u : 0u);
         }
         mma_commit(smem_u32(&sm.s_full[h]));
       };
       auto issue_pv = [&](int h, int st, bool first) {
-        const uint32_t v_base = smem_u32(sm.v[st]);
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
-          mma_bf16_ts(tmem + kColO + h * D, tmem + h * BN + kk * 8, desc_sw128(v_base + kk * 16 * 128, BN * 128, 1024),
-                      kIdescO, (kk > 0 || !first) ? 1u : 0u);
+          mma_bf16_ts(tmem + kColO + h * D, tmem + h * BN + kk * 8, dv[st] + ((kk * 16 * 128) >> 4), kIdescO,
+                      (kk > 0 || !first) ? 1u : 0u);
         mma_commit(smem_u32(&sm.pv_done[h]));
       };
       for (int ti = 0; ti < 2 && ok; ++ti) {
