@@ -60,24 +60,29 @@ constexpr float kLn2 = 0.6931471805599453f;
 
 // ------------------------------------------------------------------ schedule
 struct Sched {
-  int N, c, nt, causal;
+  int N, c, nt, causal;  // ranks, chunk length, 128-row query tiles per chunk, causal flag
+  int bnk, ntk;          // key tile length and key tiles per chunk
 };
 
 // Iterates the K/V tiles one query tile (chunk qc, tile qi) meets, in ring
-// order.  kind: 0 = every pair visible, 1 = diagonal tile (mask j <= i).
+// order: ranks s = r, r-1, ..., each rank's head chunk s, then its tail chunk
+// 2N-1-s.  Under the causal mask chunks after qc are skipped and, in qc itself,
+// only key tiles that start at or before the tile's last query are visited.
 struct KvIter {
-  int N, nt, causal, qc, qi, r;
+  int N, ntk, causal, qc, r, diag_lim;
   int t, h, ki;
-  __device__ void init(const Sched& s, int qc_, int qi_) {
-    N = s.N; nt = s.nt; causal = s.causal; qc = qc_; qi = qi_;
+  __device__ void init(const Sched& s, int qc_, int qi) {
+    N = s.N; ntk = s.ntk; causal = s.causal; qc = qc_;
     r = qc < N ? qc : 2 * N - 1 - qc;
+    const int q_valid = min(BM, s.c - qi * BM);
+    diag_lim = min(ntk, (qi * BM + q_valid - 1) / s.bnk + 1);
     t = 0; h = 0; ki = -1;
   }
   __device__ bool next(int& kc, int& kt) {
     while (t < N) {
       const int s = (r - t + N) % N;             // rank whose block is held at step t
       const int ch = h == 0 ? s : 2 * N - 1 - s;  // its head, then its tail chunk
-      const int lim = !causal ? nt : (ch < qc ? nt : (ch == qc ? qi + 1 : 0));
+      const int lim = !causal ? ntk : (ch < qc ? ntk : (ch == qc ? diag_lim : 0));
       ++ki;
       if (ki < lim) { kc = ch; kt = ki; return true; }
       ki = -1;
@@ -88,7 +93,19 @@ struct KvIter {
 };
 
 __device__ __forceinline__ int n_kv_tiles(const Sched& s, int qc, int qi) {
-  return s.causal ? qc * s.nt + qi + 1 : 2 * s.N * s.nt;
+  if (!s.causal) return 2 * s.N * s.ntk;
+  const int q_valid = min(BM, s.c - qi * BM);
+  return qc * s.ntk + min(s.ntk, (qi * BM + q_valid - 1) / s.bnk + 1);
+}
+
+// Causal mask of key tile (kc, kt) for query row `row` of tile (qc, qi):
+// the number of leading visible columns and whether any column is masked.
+__device__ __forceinline__ void tile_mask(const Sched& s, int qc, int qi, int kc, int kt, int row, int& col_lim,
+                                          bool& masked) {
+  const int kv_valid = min(s.bnk, s.c - kt * s.bnk);
+  const bool same = s.causal && kc == qc;
+  col_lim = same ? min(kv_valid, qi * BM + row - kt * s.bnk + 1) : kv_valid;
+  masked = (same && kt * s.bnk + kv_valid - 1 > qi * BM) || kv_valid < s.bnk;
 }
 
 struct Params {
@@ -217,8 +234,10 @@ __device__ __forceinline__ void chunk_exp_pack(const uint32_t (&x)[32], uint64_t
 // any row of the warp finds a score above max + 8 (log2), the warp falls back
 // to two passes (max, then exps) and the rows that grew move their reference.
 // The stale reference is exact because l and O always share it; 2^8 bounds P.
+template <int NP>
 __device__ __forceinline__ float softmax_row(uint32_t s_addr, int j, bool masked, int col_lim, float scale,
-                                             float& m, float& l, uint32_t (&pk)[BN / 2]) {
+                                             float& m, float& l, uint32_t (&pk)[NP]) {
+  constexpr int NCOL = 2 * NP;
   const uint64_t sc2 = f2pack(scale, scale);
   if (j > 0) {
     const float thr = (m + 8.f) / scale;   // raw-score threshold of a rescale
@@ -230,14 +249,14 @@ __device__ __forceinline__ float softmax_row(uint32_t s_addr, int j, bool masked
     tmem_ld32(s_addr, xa);
     tmem_wait_ld();
 #pragma unroll
-    for (int c = 0; c < BN / 32; ++c) {
+    for (int c = 0; c < NCOL / 32; ++c) {
       uint32_t (&x)[32] = (c & 1) ? xb : xa;
       uint32_t (&y)[32] = (c & 1) ? xa : xb;
-      if (c + 1 < BN / 32) tmem_ld32(s_addr + 32 * (c + 1), y);
+      if (c + 1 < NCOL / 32) tmem_ld32(s_addr + 32 * (c + 1), y);
       const float cm = chunk_mask_max(x, 32 * c, masked, col_lim);
       if (__any_sync(0xffffffffu, cm > thr)) { grow = true; tmem_wait_ld(); break; }
       chunk_exp_pack(x, sc2, negm2, acc0, acc1, &pk[16 * c]);
-      if (c + 1 < BN / 32) tmem_wait_ld();
+      if (c + 1 < NCOL / 32) tmem_wait_ld();
     }
     if (!grow) {
       float a0, a1, b0, b1;
@@ -250,7 +269,7 @@ __device__ __forceinline__ float softmax_row(uint32_t s_addr, int j, bool masked
   // two passes: the row max, then the exps against the (possibly new) reference
   float mx = -CUDART_INF_F;
 #pragma unroll
-  for (int c = 0; c < BN / 32; ++c) {
+  for (int c = 0; c < NCOL / 32; ++c) {
     uint32_t x[32];
     tmem_ld32(s_addr + 32 * c, x);
     tmem_wait_ld();
@@ -264,7 +283,7 @@ __device__ __forceinline__ float softmax_row(uint32_t s_addr, int j, bool masked
   const uint64_t negm2 = f2pack(-m_ref, -m_ref);
   uint64_t acc0 = f2pack(0.f, 0.f), acc1 = acc0;
 #pragma unroll
-  for (int c = 0; c < BN / 32; ++c) {
+  for (int c = 0; c < NCOL / 32; ++c) {
     uint32_t x[32];
     tmem_ld32(s_addr + 32 * c, x);
     tmem_wait_ld();
@@ -293,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   Smem<D>& sm = *reinterpret_cast<Smem<D>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const Item it = decode_item(p, blockIdx.x);
-  const Sched sch{p.N, p.c, p.nt, p.causal};
+  const Sched sch{p.N, p.c, p.nt, p.causal, BN, p.nt};
   volatile int* abort_flag = &sm.abort_flag;
   const long long lim = p.wait_limit;
 
@@ -455,14 +474,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < nkv; ++j) {
         int kc = 0, kt = 0;
         kv.next(kc, kt);
-        const int kv_valid = min(BN, p.c - kt * BN);
-        const bool diag = p.causal && kc == qc && kt == qi;
         const int sb = s_cnt & 1;
         const uint32_t sph = (s_cnt >> 1) & 1;
         if (!(ok = mbar_wait(smem_u32(&sm.s_full[sb]), sph, abort_flag, lim, 20))) break;
         tc_fence_after();
-        const int col_lim = diag ? min(kv_valid, row + 1) : kv_valid;
-        const bool masked = diag || kv_valid < BN;
+        int col_lim;
+        bool masked;
+        tile_mask(sch, qc, qi, kc, kt, row, col_lim, masked);
         uint32_t pk[BN / 2];
         const float alpha = softmax_row(t_lane + kColS0 + sb * BN, j, masked, col_lim, p.scale_log2, m, l, pk);
         tc_fence_before();
@@ -594,7 +612,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const Item2 it = decode_item2(p, blockIdx.x);
   const Item it1{it.b, it.hq0, it.g, it.r, it.j};   // for tile_of()
-  const Sched sch{p.N, p.c, p.nt, p.causal};
+  const Sched sch{p.N, p.c, p.nt, p.causal, BN, p.nt};
   volatile int* abort_flag = &sm.abort_flag;
   const long long lim = p.wait_limit;
 
@@ -773,13 +791,12 @@ __global__ void __launch_bounds__(kThreads2, 1)
       for (int j = 0; j < nkv; ++j) {
         int kc = 0, kt = 0;
         kv.next(kc, kt);
-        const int kv_valid = min(BN, p.c - kt * BN);
-        const bool diag = p.causal && kc == qc && kt == qi;
         if (!(ok = mbar_wait(smem_u32(&sm.s_full[h]), s_cnt & 1, abort_flag, lim, 120 + h))) break;
         ++s_cnt;
         tc_fence_after();
-        const int col_lim = diag ? min(kv_valid, row + 1) : kv_valid;
-        const bool masked = diag || kv_valid < BN;
+        int col_lim;
+        bool masked;
+        tile_mask(sch, qc, qi, kc, kt, row, col_lim, masked);
         uint32_t pk[BN / 2];
         const float alpha = softmax_row(t_lane + colS, j, masked, col_lim, p.scale_log2, m, l, pk);
         if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
@@ -841,7 +858,288 @@ __global__ void __launch_bounds__(kThreads2, 1)
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-// Per-rank tile classification with the kernel's own iterator (for tests).
+// ===========================================================================
+// Variant 3: two GQA heads per CTA with 64-key K/V tiles and double-buffered
+// score tiles.  Tensor memory: S[h][b] = cols [64*(2h+b), +64) for head h and
+// buffer b, O[h] = cols [256 + D*h, +D).  P[h][b] (bf16 pairs) overwrites the
+// first 32 columns of S[h][b] and feeds P.V from tensor memory.  Because every
+// head has two score buffers, the MMA thread issues the scores of K/V tile j+2
+// as soon as P.V of tile j has been issued (same buffer, in-order execution),
+// so the tensor core always holds queued work while a softmax round trip is in
+// flight.  Issue order per tile j: PV0_j, PV1_j, S0_{j+2}, S1_{j+2}.
+// Shared memory: Q of both heads, a four-stage ring of 64-row K and V tiles.
+// ===========================================================================
+constexpr int BN3 = 64;
+constexpr int STAGES3 = 4;
+constexpr int kThreads3 = 384;
+
+template <int D>
+struct __align__(1024) Smem3 {
+  uint8_t q[2][BM * D * 2];
+  uint8_t k[STAGES3][BN3 * D * 2];
+  uint8_t v[STAGES3][BN3 * D * 2];
+  uint64_t q_full, q_empty, k_full[STAGES3], k_empty[STAGES3], v_full[STAGES3], v_empty[STAGES3];
+  uint64_t s_full[2][2], p_full[2][2], pv_done[2], o_empty[2], drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads3, 1)
+    ring_attn_bf16_pair64_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                                 const __grid_constant__ CUtensorMap tmV, const Params p) {
+  constexpr int SLABS = D / 64;
+  constexpr uint32_t kQBytes = BM * D * 2;
+  constexpr uint32_t kKVBytes = BN3 * D * 2;
+  constexpr uint32_t kIdescS = idesc_bf16_f32(BM, BN3, 0, 0);
+  constexpr uint32_t kIdescO = idesc_bf16_f32(BM, D, 0, 1);
+  constexpr uint32_t kColO3 = 4 * BN3;
+
+  extern __shared__ uint8_t smem_raw[];
+  Smem3<D>& sm = *reinterpret_cast<Smem3<D>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const Item2 it = decode_item2(p, blockIdx.x);
+  const Item it1{it.b, it.hq0, it.g, it.r, it.j};
+  const Sched sch{p.N, p.c, p.nt, p.causal, BN3, static_cast<int>((p.c + BN3 - 1) / BN3)};
+  volatile int* abort_flag = &sm.abort_flag;
+  const long long lim = p.wait_limit;
+
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&sm.q_full), 1);
+    mbar_init(smem_u32(&sm.q_empty), 1);
+    for (int s = 0; s < STAGES3; ++s) {
+      mbar_init(smem_u32(&sm.k_full[s]), 1);
+      mbar_init(smem_u32(&sm.k_empty[s]), 1);
+      mbar_init(smem_u32(&sm.v_full[s]), 1);
+      mbar_init(smem_u32(&sm.v_empty[s]), 1);
+    }
+    for (int h = 0; h < 2; ++h) {
+      for (int b = 0; b < 2; ++b) {
+        mbar_init(smem_u32(&sm.s_full[h][b]), 1);
+        mbar_init(smem_u32(&sm.p_full[h][b]), 128);
+      }
+      mbar_init(smem_u32(&sm.pv_done[h]), 1);
+      mbar_init(smem_u32(&sm.o_empty[h]), 128);
+    }
+    mbar_init(smem_u32(&sm.drain), 1);
+    sm.abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&sm.tmem_base), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+
+  if (warp == 0) {
+    // ============================================================ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      uint32_t kv_cnt = 0;
+      bool ok = true;
+      for (int ti = 0; ti < 2 && ok; ++ti) {
+        int qc, qi;
+        tile_of(p, it1, ti, qc, qi);
+        if (!(ok = mbar_wait(smem_u32(&sm.q_empty), (ti & 1) ^ 1, abort_flag, lim, 201))) break;
+        const uint32_t qb = smem_u32(&sm.q_full);
+        mbar_arrive_expect_tx(qb, 2 * kQBytes);
+        const int32_t qrow = static_cast<int32_t>(token_row(p, it.b, qc, qi * BM));
+        for (int h = 0; h < 2; ++h)
+          for (int s = 0; s < SLABS; ++s)
+            tma_load_3d(smem_u32(sm.q[h] + s * BM * 128), &tmQ, qb, 64 * s, it.hq0 + h, qrow);
+        KvIter kv;
+        kv.init(sch, qc, qi);
+        int kc, kt;
+        while (kv.next(kc, kt)) {
+          const int st = kv_cnt % STAGES3;
+          const uint32_t ph = (kv_cnt / STAGES3) & 1;
+          const int32_t krow = static_cast<int32_t>(token_row(p, it.b, kc, kt * BN3));
+          if (!(ok = mbar_wait(smem_u32(&sm.k_empty[st]), ph ^ 1, abort_flag, lim, 202))) break;
+          mbar_arrive_expect_tx(smem_u32(&sm.k_full[st]), kKVBytes);
+          for (int s = 0; s < SLABS; ++s)
+            tma_load_3d(smem_u32(sm.k[st] + s * BN3 * 128), &tmK, smem_u32(&sm.k_full[st]), 64 * s, it.g, krow);
+          if (!(ok = mbar_wait(smem_u32(&sm.v_empty[st]), ph ^ 1, abort_flag, lim, 203))) break;
+          mbar_arrive_expect_tx(smem_u32(&sm.v_full[st]), kKVBytes);
+          for (int s = 0; s < SLABS; ++s)
+            tma_load_3d(smem_u32(sm.v[st] + s * BN3 * 128), &tmV, smem_u32(&sm.v_full[st]), 64 * s, it.g, krow);
+          ++kv_cnt;
+        }
+      }
+      if (!ok) {
+        // let the copies already in flight land before the CTA exits
+        for (int back = 1; back <= STAGES3 && back <= static_cast<int>(kv_cnt); ++back) {
+          const uint32_t c = kv_cnt - back;
+          mbar_wait(smem_u32(&sm.k_full[c % STAGES3]), (c / STAGES3) & 1, abort_flag, 1 << 22, 0);
+          mbar_wait(smem_u32(&sm.v_full[c % STAGES3]), (c / STAGES3) & 1, abort_flag, 1 << 22, 0);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ============================================================ MMA issuer
+    if (lane == 0) {
+      uint32_t kv_cnt = 0;
+      bool ok = true;
+      const uint64_t dq[2] = {desc_sw128(smem_u32(sm.q[0]), 16, 1024), desc_sw128(smem_u32(sm.q[1]), 16, 1024)};
+      uint64_t dk[STAGES3], dv[STAGES3];
+      for (int s = 0; s < STAGES3; ++s) {
+        dk[s] = desc_sw128(smem_u32(sm.k[s]), 16, 1024);
+        dv[s] = desc_sw128(smem_u32(sm.v[s]), BN3 * 128, 1024);
+      }
+      // S[h][b] = Q_h K^T of the tile in stage st
+      auto issue_s = [&](int h, int st, int b) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_bf16_ss(tmem + (2 * h + b) * BN3, dq[h] + ((((kk >> 2) * (BM * 128)) + (kk & 3) * 32) >> 4),
+                      dk[st] + ((((kk >> 2) * (BN3 * 128)) + (kk & 3) * 32) >> 4), kIdescS, kk > 0 ? 1u : 0u);
+        mma_commit(smem_u32(&sm.s_full[h][b]));
+      };
+      // O_h += P[h][b] V of the tile in stage st
+      auto issue_pv = [&](int h, int st, int b, bool first) {
+#pragma unroll
+        for (int kk = 0; kk < BN3 / 16; ++kk)
+          mma_bf16_ts(tmem + kColO3 + h * D, tmem + (2 * h + b) * BN3 + kk * 8, dv[st] + ((kk * 16 * 128) >> 4),
+                      kIdescO, (kk > 0 || !first) ? 1u : 0u);
+        mma_commit(smem_u32(&sm.pv_done[h]));
+      };
+      for (int ti = 0; ti < 2 && ok; ++ti) {
+        int qc, qi;
+        tile_of(p, it1, ti, qc, qi);
+        const int nkv = n_kv_tiles(sch, qc, qi);
+        if (!(ok = mbar_wait(smem_u32(&sm.q_full), ti & 1, abort_flag, lim, 210))) break;
+        for (int jj = 0; jj < 2 && jj < nkv && ok; ++jj) {   // scores of the first two tiles
+          const uint32_t g = kv_cnt + jj;
+          const int st = g % STAGES3;
+          if (!(ok = mbar_wait(smem_u32(&sm.k_full[st]), (g / STAGES3) & 1, abort_flag, lim, 211))) break;
+          tc_fence_after();
+          issue_s(0, st, g & 1);
+          issue_s(1, st, g & 1);
+          mma_commit(smem_u32(&sm.k_empty[st]));
+          if (jj == nkv - 1) mma_commit(smem_u32(&sm.q_empty));
+        }
+        for (int j = 0; j < nkv && ok; ++j) {
+          const uint32_t g = kv_cnt + j;
+          const int st = g % STAGES3, b = g & 1;
+          const uint32_t ph4 = (g / STAGES3) & 1, ph2 = (g >> 1) & 1;
+          if (!(ok = mbar_wait(smem_u32(&sm.p_full[0][b]), ph2, abort_flag, lim, 212))) break;
+          if (!(ok = mbar_wait(smem_u32(&sm.v_full[st]), ph4, abort_flag, lim, 213))) break;
+          if (j == 0 && !(ok = mbar_wait(smem_u32(&sm.o_empty[0]), (ti & 1) ^ 1, abort_flag, lim, 214))) break;
+          tc_fence_after();
+          issue_pv(0, st, b, j == 0);
+          if (!(ok = mbar_wait(smem_u32(&sm.p_full[1][b]), ph2, abort_flag, lim, 215))) break;
+          if (j == 0 && !(ok = mbar_wait(smem_u32(&sm.o_empty[1]), (ti & 1) ^ 1, abort_flag, lim, 216))) break;
+          tc_fence_after();
+          issue_pv(1, st, b, j == 0);
+          mma_commit(smem_u32(&sm.v_empty[st]));
+          if (j + 2 < nkv) {   // scores of tile j+2 into the buffer P.V_j just consumed
+            const uint32_t g2 = g + 2;
+            const int st2 = g2 % STAGES3;
+            if (!(ok = mbar_wait(smem_u32(&sm.k_full[st2]), (g2 / STAGES3) & 1, abort_flag, lim, 217))) break;
+            tc_fence_after();
+            issue_s(0, st2, b);
+            issue_s(1, st2, b);
+            mma_commit(smem_u32(&sm.k_empty[st2]));
+            if (j + 2 == nkv - 1) mma_commit(smem_u32(&sm.q_empty));
+          }
+        }
+        kv_cnt += nkv;
+      }
+      mma_commit(smem_u32(&sm.drain));
+      mbar_wait(smem_u32(&sm.drain), 0, abort_flag, ok ? lim : (1 << 22), 218);
+    }
+  } else if (warp >= 4) {
+    // ============================================================ softmax + epilogue (head h)
+    const int h = (warp - 4) >> 2;
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const uint32_t colO = kColO3 + h * D;
+    const int hq = it.hq0 + h;
+    uint32_t cnt = 0, pv_base = 0;
+    bool ok = true;
+    for (int ti = 0; ti < 2 && ok; ++ti) {
+      int qc, qi;
+      tile_of(p, it1, ti, qc, qi);
+      const int q_valid = min(BM, p.c - qi * BM);
+      const int nkv = n_kv_tiles(sch, qc, qi);
+      KvIter kv;
+      kv.init(sch, qc, qi);
+      float m = -CUDART_INF_F, l = 0.f;
+      for (int j = 0; j < nkv; ++j, ++cnt) {
+        int kc = 0, kt = 0;
+        kv.next(kc, kt);
+        const int b = cnt & 1;
+        const uint32_t colS = (2 * h + b) * BN3;
+        if (!(ok = mbar_wait(smem_u32(&sm.s_full[h][b]), (cnt >> 1) & 1, abort_flag, lim, 220 + h))) break;
+        tc_fence_after();
+        int col_lim;
+        bool masked;
+        tile_mask(sch, qc, qi, kc, kt, row, col_lim, masked);
+        uint32_t pk[BN3 / 2];
+        const float alpha = softmax_row(t_lane + colS, j, masked, col_lim, p.scale_log2, m, l, pk);
+        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+          // O_h must hold P.V of every earlier tile before it is rescaled
+          if (!(ok = mbar_wait(smem_u32(&sm.pv_done[h]), (pv_base + j - 1) & 1, abort_flag, lim, 224 + h))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int c4 = 0; c4 < D / 32; ++c4) {
+            uint32_t orr[32];
+            tmem_ld32(t_lane + colO + 32 * c4, orr);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
+            tmem_st32(t_lane + colO + 32 * c4, orr);
+          }
+        }
+        tmem_st32(t_lane + colS, pk);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(smem_u32(&sm.p_full[h][b]));
+      }
+      if (!ok) break;
+      // ---------------------------------------------------------- epilogue
+      if (!(ok = mbar_wait(smem_u32(&sm.pv_done[h]), (pv_base + nkv - 1) & 1, abort_flag, lim, 226 + h))) break;
+      pv_base += nkv;
+      tc_fence_after();
+      const float inv_l = l > 0.f ? 1.f / l : 0.f;
+      const bool row_ok = row < q_valid;
+      const int64_t trow = token_row(p, it.b, qc, qi * BM + row);
+      __nv_bfloat16* orow = p.o + (trow * p.Hq + hq) * D;
+#pragma unroll
+      for (int c4 = 0; c4 < D / 32; ++c4) {
+        uint32_t orr[32];
+        tmem_ld32(t_lane + colO + 32 * c4, orr);
+        tmem_wait_ld();
+        if (row_ok) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 8) {
+            uint4 pk4;
+            pk4.x = f2_bf16x2(__uint_as_float(orr[i]) * inv_l, __uint_as_float(orr[i + 1]) * inv_l);
+            pk4.y = f2_bf16x2(__uint_as_float(orr[i + 2]) * inv_l, __uint_as_float(orr[i + 3]) * inv_l);
+            pk4.z = f2_bf16x2(__uint_as_float(orr[i + 4]) * inv_l, __uint_as_float(orr[i + 5]) * inv_l);
+            pk4.w = f2_bf16x2(__uint_as_float(orr[i + 6]) * inv_l, __uint_as_float(orr[i + 7]) * inv_l);
+            *reinterpret_cast<uint4*>(orow + 32 * c4 + i) = pk4;
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(smem_u32(&sm.o_empty[h]));
+      if (row_ok) p.lse[trow * p.Hq + hq] = l > 0.f ? (m + log2f(l)) * kLn2 : -CUDART_INF_F;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+// Per-rank tile classification with the kernels' own iterator (for tests):
+// visited tiles that need no mask, visited tiles with a causal mask, skipped.
 __global__ void schedule_counts_kernel(Sched s, unsigned long long* counts) {
   const int n_tiles = 2 * s.N * s.nt;  // query tiles of the whole sequence
   for (int idx = blockIdx.x * blockDim.x + threadIdx.x; idx < n_tiles; idx += gridDim.x * blockDim.x) {
@@ -853,14 +1151,14 @@ __global__ void schedule_counts_kernel(Sched s, unsigned long long* counts) {
     unsigned long long full = 0, diag = 0, seen = 0;
     while (kv.next(kc, kt)) {
       ++seen;
-      const int qv = min(BM, s.c - qi * BM), kvv = min(BN, s.c - kt * BN);
-      const bool d = s.causal && kc == qc && kt == qi && !(qv == 1 && kvv == 1);
+      const int kvv = min(s.bnk, s.c - kt * s.bnk);
+      const bool d = s.causal && kc == qc && kt * s.bnk + kvv - 1 > qi * BM;
       if (d) ++diag; else ++full;
     }
     if (static_cast<int>(seen) != n_kv_tiles(s, qc, qi)) ra_record_error(RA_ERR_DEVICE_BOUNDS, 30);
     atomicAdd(&counts[r * 3 + 0], full);
     atomicAdd(&counts[r * 3 + 1], diag);
-    atomicAdd(&counts[r * 3 + 2], static_cast<unsigned long long>(2 * s.N * s.nt) - seen);
+    atomicAdd(&counts[r * 3 + 2], static_cast<unsigned long long>(2 * s.N * s.ntk) - seen);
   }
 }
 
@@ -884,12 +1182,12 @@ EncodeTiledFn get_encode_fn() {
 
 // Token-major [rows, H, D] bf16 tensor; box = 64 columns x 1 head x 128 rows,
 // 128-byte swizzle (the layout the MMA descriptors expect).
-ra_status make_map(CUtensorMap* map, const void* base, int D, int H, int64_t rows) {
+ra_status make_map(CUtensorMap* map, const void* base, int D, int H, int64_t rows, uint32_t box_rows = 128) {
   EncodeTiledFn enc = get_encode_fn();
   if (!enc) return ra::fail(RA_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(H) * D * 2};
-  cuuint32_t box[3] = {64, 1, 128};
+  cuuint32_t box[3] = {64, 1, box_rows};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -908,6 +1206,18 @@ ra_status launch_bf16(const void* q, const void* k, const void* v, const Params&
   if ((st = make_map(&mk, k, D, prm.Hkv, rows)) != RA_OK) return st;
   if ((st = make_map(&mv, v, D, prm.Hkv, rows)) != RA_OK) return st;
   const int64_t tiles = static_cast<int64_t>(prm.B) * prm.Hq * prm.N * prm.nt;  // mirrored tile pairs x heads
+  if (variant == 3) {
+    CUtensorMap mk64, mv64;
+    if ((st = make_map(&mk64, k, D, prm.Hkv, rows, BN3)) != RA_OK) return st;
+    if ((st = make_map(&mv64, v, D, prm.Hkv, rows, BN3)) != RA_OK) return st;
+    const size_t smem = sizeof(Smem3<D>) + 1024;
+    RA_CUDA_TRY(cudaFuncSetAttribute(ring_attn_bf16_pair64_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(smem)));
+    ring_attn_bf16_pair64_kernel<D><<<static_cast<unsigned>(tiles / 2), kThreads3, smem, stream>>>(mq, mk64, mv64,
+                                                                                                 prm);
+    RA_LAUNCH_CHECK("ring_attn_bf16_pair64_kernel");
+    return RA_OK;
+  }
   if (variant == 2) {
     const size_t smem = sizeof(Smem2<D>) + 1024;
     RA_CUDA_TRY(cudaFuncSetAttribute(ring_attn_bf16_pair_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -948,7 +1258,7 @@ extern "C" ra_status ra_ring_attn_fwd_ex(const void* q, const void* k, const voi
                                          int32_t causal, int32_t n_ranks, float scale, ra_layout layout,
                                          int32_t variant, ra_stream stream) {
   ra::clear_error();
-  RA_REQUIRE(variant >= 0 && variant <= 2, "variant must be 0, 1 or 2");
+  RA_REQUIRE(variant >= 0 && variant <= 3, "variant must be 0, 1, 2 or 3");
   RA_REQUIRE(B >= 1 && Hq >= 1 && Hkv >= 1 && S >= 1, "B, Hq, Hkv, S must be >= 1");
   RA_REQUIRE(Hq % Hkv == 0, "Hq (%d) must be a multiple of Hkv (%d)", Hq, Hkv);
   RA_REQUIRE(n_ranks >= 1, "n_ranks must be >= 1 (got %d)", n_ranks);
@@ -974,8 +1284,8 @@ extern "C" ra_status ra_ring_attn_fwd_ex(const void* q, const void* k, const voi
   prm.wait_limit = ra::wait_limit();
   const int64_t items = static_cast<int64_t>(B) * Hkv * n_ranks * prm.nt * prm.group;
   RA_REQUIRE(items < (int64_t(1) << 31), "too many work items");
-  if (variant == 0) variant = (prm.group % 2 == 0) ? 2 : 1;
-  RA_REQUIRE(variant == 1 || prm.group % 2 == 0, "the two-head variant needs an even Hq/Hkv");
+  if (variant == 0) variant = (prm.group % 2 == 0) ? 3 : 1;
+  RA_REQUIRE(variant == 1 || prm.group % 2 == 0, "the two-head variants need an even Hq/Hkv");
   if (d == 128) return launch_bf16<128>(q, k, v, prm, variant, stream);
   return launch_bf16<64>(q, k, v, prm, variant, stream);
 }
@@ -986,16 +1296,24 @@ extern "C" ra_status ra_ring_attn_fwd(const void* q, const void* k, const void* 
   return ra_ring_attn_fwd_ex(q, k, v, o, lse, B, Hq, Hkv, S, d, dt, causal, n_ranks, scale, layout, 0, stream);
 }
 
-extern "C" ra_status ra_ring_schedule_counts(int32_t S, int32_t n_ranks, int32_t causal, int64_t* counts,
-                                             ra_stream stream) {
+extern "C" ra_status ra_ring_schedule_counts_ex(int32_t S, int32_t n_ranks, int32_t causal, int32_t kv_tile,
+                                                int64_t* counts, ra_stream stream) {
   ra::clear_error();
   RA_REQUIRE(n_ranks >= 1 && S >= 1 && S % (2 * n_ranks) == 0, "S must be a positive multiple of 2*n_ranks");
+  RA_REQUIRE(kv_tile == 64 || kv_tile == 128, "kv_tile must be 64 or 128");
   RA_REQUIRE(counts != nullptr && reinterpret_cast<uintptr_t>(counts) % 8 == 0, "counts must be 8-byte aligned");
-  Sched s{n_ranks, S / (2 * n_ranks), static_cast<int>(ra::ceil_div(S / (2 * n_ranks), BM)), causal ? 1 : 0};
+  const int c = S / (2 * n_ranks);
+  Sched s{n_ranks, c, static_cast<int>(ra::ceil_div(c, BM)), causal ? 1 : 0, kv_tile,
+          static_cast<int>(ra::ceil_div(c, kv_tile))};
   RA_CUDA_TRY(cudaMemsetAsync(counts, 0, sizeof(int64_t) * 3 * n_ranks, stream));
   const int n_tiles = 2 * s.N * s.nt;
   schedule_counts_kernel<<<static_cast<unsigned>(ra::ceil_div(n_tiles, 128)), 128, 0, stream>>>(
       s, reinterpret_cast<unsigned long long*>(counts));
   RA_LAUNCH_CHECK("schedule_counts_kernel");
   return RA_OK;
+}
+
+extern "C" ra_status ra_ring_schedule_counts(int32_t S, int32_t n_ranks, int32_t causal, int64_t* counts,
+                                             ra_stream stream) {
+  return ra_ring_schedule_counts_ex(S, n_ranks, causal, 128, counts, stream);
 }

@@ -33,6 +33,7 @@ SIGNATURES = {
     "ra_ring_attn_fwd_ex": [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _c.c_int, _i32, _i32, _f32,
                             _c.c_int, _i32, _vp],
     "ra_ring_schedule_counts": [_i32, _i32, _i32, _vp, _vp],
+    "ra_ring_schedule_counts_ex": [_i32, _i32, _i32, _i32, _vp, _vp],
     "ra_lse_merge": [_vp, _vp, _i32, _i64, _i32, _i32, _vp, _c.c_int, _vp, _vp],
     "ra_cp_slot_mapping": [_vp, _vp, _vp, _i32, _i32, _i64, _i32, _i32, _i32, _i32, _vp, _vp],
     "ra_cp_kv_scatter": [_vp, _vp, _vp, _vp, _vp, _i64, _i32, _i32, _i32, _i32, _i64, _c.c_int, _vp],
@@ -152,7 +153,8 @@ def ring_attn_fwd(q, k, v, causal: bool, n_ranks: int, B: int = 1, scale: Option
     """Ring-order attention forward.  q [B*S, Hq, d], k/v [B*S, Hkv, d] token-major.
 
     Returns (O [B*S, Hq, d] in q's dtype, LSE float32 [B*S, Hq]).  ``variant`` picks the
-    bf16 kernel (0 automatic, 1 one head per CTA, 2 two GQA heads per CTA)."""
+    bf16 kernel (0 automatic, 1 one head per CTA, 2 two GQA heads per CTA, 3 two heads with 64-key
+    tiles and double-buffered scores)."""
     _need_cuda(q, k, v, o, lse)
     rows, Hq, d = q.shape
     Hkv = k.shape[1]
@@ -169,9 +171,10 @@ def ring_attn_fwd(q, k, v, causal: bool, n_ranks: int, B: int = 1, scale: Option
     return o, lse
 
 
-def ring_schedule_counts(S: int, n_ranks: int, causal: bool, device="cuda"):
+def ring_schedule_counts(S: int, n_ranks: int, causal: bool, kv_tile: int = 128, device="cuda"):
+    """Per rank: (unmasked, causally masked, skipped) (query tile, key tile) pairs of the kernels' schedule."""
     out = torch.empty((n_ranks, 3), dtype=torch.int64, device=device)
-    _check(lib().ra_ring_schedule_counts(S, n_ranks, 1 if causal else 0, _ptr(out), _stream()))
+    _check(lib().ra_ring_schedule_counts_ex(S, n_ranks, 1 if causal else 0, kv_tile, _ptr(out), _stream()))
     return out
 
 

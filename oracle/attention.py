@@ -256,26 +256,31 @@ def causal_pairs_per_rank(N: int, c: int):
     return out
 
 
-def causal_tiles_per_rank(N: int, c: int, T: int):
-    """Per rank: (full, partial, skipped) counts of T x T (query tile, key tile)
-    pairs when every chunk is cut into ceil(c/T) tiles (the last may be ragged).
+def causal_tiles_per_rank(N: int, c: int, T: int, Tk: int = None):
+    """Per rank: (full, partial, skipped) counts of (query tile, key tile) pairs
+    when every chunk is cut into query tiles of T and key tiles of Tk tokens
+    (Tk defaults to T; the last tile of a chunk may be shorter).
 
     Classification is by brute force over the positions inside each tile pair:
     'full' if every pair is visible, 'partial' if some are, 'skip' if none.
     """
-    nt = -(-c // T)
-    tiles = []
-    for ch in range(2 * N):
-        for i in range(nt):
-            lo = ch * c + i * T
-            hi = min(ch * c + c, lo + T)
-            tiles.append((ch, lo, hi))
+    Tk = T if Tk is None else Tk
+
+    def tiles(L):
+        out = []
+        for ch in range(2 * N):
+            for i in range(-(-c // L)):
+                lo = ch * c + i * L
+                out.append((ch, lo, min(ch * c + c, lo + L)))
+        return out
+
+    qtiles, ktiles = tiles(T), tiles(Tk)
     res = []
     for r in range(N):
-        mine = [t for t in tiles if t[0] in rank_chunks(N, r)]
+        mine = [t for t in qtiles if t[0] in rank_chunks(N, r)]
         full = part = skip = 0
         for (_, qlo, qhi) in mine:
-            for (_, klo, khi) in tiles:
+            for (_, klo, khi) in ktiles:
                 qs = np.arange(qlo, qhi)[:, None]
                 ks = np.arange(klo, khi)[None, :]
                 vis = _visible(qs, ks)

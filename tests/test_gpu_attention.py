@@ -67,19 +67,20 @@ def test_fp32_ragged_and_gqa(ra, S, N, causal, Hq, Hkv, d):
     (2048, 4, 1, 2, 2, 64, False),
     (16, 8, 1, 2, 2, 128, True),       # chunks of 1 token
 ])
-@pytest.mark.parametrize("variant", [1, 2])
+@pytest.mark.parametrize("variant", [1, 2, 3])
 def test_bf16_parity_small(ra, S, N, B, Hq, Hkv, d, causal, variant):
-    if variant == 2 and (Hq // Hkv) % 2:
+    if variant >= 2 and (Hq // Hkv) % 2:
         Hq = 2 * Hq                       # the two-head kernel needs an even GQA group
     q, k, v, o, lse = _run(ra, 3, B, S, Hq, Hkv, d, N, causal, torch.bfloat16, variant=variant)
     O, L = _oracle_full(q, k, v, B, S, causal)
     assert_parity(o, O, lse, L, torch.bfloat16, "bf16 v%d S=%d N=%d" % (variant, S, N))
 
 
-def test_bf16_variants_agree(ra):
+@pytest.mark.parametrize("other", [2, 3])
+def test_bf16_variants_agree(ra, other):
     B, S, Hq, Hkv, d, N = 1, 2560, 8, 2, 128, 5
     _, _, _, o1, l1 = _run(ra, 6, B, S, Hq, Hkv, d, N, True, torch.bfloat16, variant=1)
-    _, _, _, o2, l2 = _run(ra, 6, B, S, Hq, Hkv, d, N, True, torch.bfloat16, variant=2)
+    _, _, _, o2, l2 = _run(ra, 6, B, S, Hq, Hkv, d, N, True, torch.bfloat16, variant=other)
     assert (o1.float() - o2.float()).abs().max().item() <= 1.6e-2
     assert (l1 - l2).abs().max().item() <= 1e-4
 
@@ -166,14 +167,15 @@ def test_bf16_long_context_131k(ra):
 # --------------------------------------------------------------------- schedule
 
 @pytest.mark.parametrize("S,N", [(512, 2), (640, 2), (8192, 8), (1200, 3), (16, 8), (2 * 16 * 300, 16)])
-def test_schedule_counts_match_brute_force(ra, S, N):
+@pytest.mark.parametrize("kv_tile", [128, 64])
+def test_schedule_counts_match_brute_force(ra, S, N, kv_tile):
     c = S // (2 * N)
-    got = ra.ring_schedule_counts(S, N, True).cpu().tolist()
+    got = ra.ring_schedule_counts(S, N, True, kv_tile).cpu().tolist()
     check_status(ra)
-    assert got == [list(x) for x in oracle.causal_tiles_per_rank(N, c, 128)]
-    nt = -(-c // 128)
-    got_nc = ra.ring_schedule_counts(S, N, False).cpu().tolist()
-    assert got_nc == [[2 * nt * 2 * N * nt, 0, 0]] * N
+    assert got == [list(x) for x in oracle.causal_tiles_per_rank(N, c, 128, kv_tile)]
+    nt, ntk = -(-c // 128), -(-c // kv_tile)
+    got_nc = ra.ring_schedule_counts(S, N, False, kv_tile).cpu().tolist()
+    assert got_nc == [[2 * nt * 2 * N * ntk, 0, 0]] * N
 
 
 # --------------------------------------------------------------------- failure detection

@@ -273,6 +273,21 @@ def test_causal_tiles_closed_form(N, c, T):
     assert oracle.causal_tiles_per_rank(N, c, T) == [(full, part, skip)] * N
 
 
+@pytest.mark.parametrize("N,c", [(2, 256), (3, 384), (1, 128)])
+def test_causal_tiles_half_key_tiles_closed_form(N, c):
+    """Query tiles of 128 and key tiles of 64 (tile-aligned chunks): a query tile i of
+    chunk a sees 2*a*nt full key tiles before its chunk, 2*i full ones inside it, and
+    two partial (diagonal) key tiles."""
+    nt = c // 128
+    res = oracle.causal_tiles_per_rank(N, c, 128, 64)
+    for r in range(N):
+        chunks = oracle.rank_chunks(N, r)
+        full = sum(2 * a * nt + 2 * i for a in chunks for i in range(nt))
+        part = 2 * 2 * nt
+        skip = 2 * nt * 2 * N * 2 * nt - full - part
+        assert res[r] == (full, part, skip)
+
+
 def test_causal_tiles_ragged_totals():
     N, c, T = 2, 5, 2          # tiles of 2,2,1 per chunk
     res = oracle.causal_tiles_per_rank(N, c, T)
