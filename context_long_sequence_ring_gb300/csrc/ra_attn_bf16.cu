@@ -879,7 +879,7 @@ struct __align__(1024) Smem3 {
   uint8_t k[STAGES3][BN3 * D * 2];
   uint8_t v[STAGES3][BN3 * D * 2];
   uint64_t q_full, q_empty, k_full[STAGES3], k_empty[STAGES3], v_full[STAGES3], v_empty[STAGES3];
-  uint64_t s_full[2][2], p_full[2][2], pv_done[2], o_empty[2], drain;
+  uint64_t s_full[2][2], p_full[2][2], pv_done[2], o_full[2], o_empty[2], drain;
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -919,6 +919,7 @@ __global__ void __launch_bounds__(kThreads3, 1)
         mbar_init(smem_u32(&sm.p_full[h][b]), 128);
       }
       mbar_init(smem_u32(&sm.pv_done[h]), 1);
+      mbar_init(smem_u32(&sm.o_full[h]), 1);
       mbar_init(smem_u32(&sm.o_empty[h]), 128);
     }
     mbar_init(smem_u32(&sm.drain), 1);
@@ -1030,10 +1031,12 @@ __global__ void __launch_bounds__(kThreads3, 1)
           if (j == 0 && !(ok = mbar_wait(smem_u32(&sm.o_empty[0]), (ti & 1) ^ 1, abort_flag, lim, 214))) break;
           tc_fence_after();
           issue_pv(0, st, b, j == 0);
+          if (j == nkv - 1) mma_commit(smem_u32(&sm.o_full[0]));
           if (!(ok = mbar_wait(smem_u32(&sm.p_full[1][b]), ph2, abort_flag, lim, 215))) break;
           if (j == 0 && !(ok = mbar_wait(smem_u32(&sm.o_empty[1]), (ti & 1) ^ 1, abort_flag, lim, 216))) break;
           tc_fence_after();
           issue_pv(1, st, b, j == 0);
+          if (j == nkv - 1) mma_commit(smem_u32(&sm.o_full[1]));
           mma_commit(smem_u32(&sm.v_empty[st]));
           if (j + 2 < nkv) {   // scores of tile j+2 into the buffer P.V_j just consumed
             const uint32_t g2 = g + 2;
@@ -1102,7 +1105,10 @@ __global__ void __launch_bounds__(kThreads3, 1)
       }
       if (!ok) break;
       // ---------------------------------------------------------- epilogue
-      if (!(ok = mbar_wait(smem_u32(&sm.pv_done[h]), (pv_base + nkv - 1) & 1, abort_flag, lim, 226 + h))) break;
+      // o_full completes once per query tile, after its last P.V: the per-P.V
+      // barrier may lag two phases here (scores run two tiles ahead), so its
+      // parity cannot be used for this wait.
+      if (!(ok = mbar_wait(smem_u32(&sm.o_full[h]), ti & 1, abort_flag, lim, 226 + h))) break;
       pv_base += nkv;
       tc_fence_after();
       const float inv_l = l > 0.f ? 1.f / l : 0.f;
@@ -1284,7 +1290,7 @@ extern "C" ra_status ra_ring_attn_fwd_ex(const void* q, const void* k, const voi
   prm.wait_limit = ra::wait_limit();
   const int64_t items = static_cast<int64_t>(B) * Hkv * n_ranks * prm.nt * prm.group;
   RA_REQUIRE(items < (int64_t(1) << 31), "too many work items");
-  if (variant == 0) variant = (prm.group % 2 == 0) ? 3 : 1;
+  if (variant == 0) variant = (prm.group % 2 == 0) ? 2 : 1;
   RA_REQUIRE(variant == 1 || prm.group % 2 == 0, "the two-head variants need an even Hq/Hkv");
   if (d == 128) return launch_bf16<128>(q, k, v, prm, variant, stream);
   return launch_bf16<64>(q, k, v, prm, variant, stream);

@@ -129,7 +129,7 @@ ra_status ra_ring_attn_fwd(const void* q, const void* k, const void* v, void* o,
                            ra_layout layout, ra_stream stream);
 
 /* Same as ra_ring_attn_fwd with an explicit bf16 kernel variant:
- * 0 = automatic (3 when Hq/Hkv is even, else 1);
+ * 0 = automatic (2 when Hq/Hkv is even, else 1);
  * 1 = one query head per CTA (mirrored pair of query tiles, 128-key tiles,
  *     P via shared memory);
  * 2 = two query heads of one GQA group per CTA sharing every 128-key K/V tile
