@@ -559,15 +559,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ===========================================================================
 // Two-head variant for GQA (Hq/Hkv even): a CTA runs two query heads that read
 // the same K/V head, so every K/V tile TMA brings in feeds two score tiles.
-// Roles (384 threads): warp 0 TMA, warp 1 TMEM allocation + MMA issue, warps
-// 4..7 softmax of head 0, warps 8..11 softmax of head 1 (warps 2, 3 idle).
+// Roles (384 threads): warp 0 TMA, warp 1 TMEM allocation + MMA issue for head
+// 0, warp 2 MMA issue for head 1, warps 4..7 softmax of head 0, warps 8..11
+// softmax of head 1 (warp 3 idle).
 // Tensor memory: S_h = cols [128h, 128h+128), O_h = cols [256+128h, ...).
 // P_h (bf16, two per column) overwrites the first 64 columns of S_h and is
 // the A operand of O_h += P_h V straight from tensor memory, so P never
-// touches shared memory.  MMA issue order per K/V tile j:
-//   PV0_j, S0_{j+1}, PV1_j, S1_{j+1}
-// (tcgen05 operations of one thread execute in issue order, so S_h{j+1} may
-// overwrite the columns PV_h_j reads).  A softmax warpgroup only waits for
+// touches shared memory.  Each head's issuer runs PV_h(j), S_h(j+1), ...
+// (tcgen05 operations of one thread execute in issue order, so S_h(j+1) may
+// overwrite the columns PV_h(j) reads).  A softmax warpgroup only waits for
 // the previous P.V when it must rescale O (lazy rescale, threshold 2^8).
 // ===========================================================================
 struct Item2 {
@@ -591,7 +591,7 @@ struct __align__(1024) Smem2 {
   uint8_t k[STAGES][BN * D * 2];
   uint8_t v[STAGES][BN * D * 2];
   uint64_t q_full, q_empty, k_full[STAGES], k_empty[STAGES], v_full[STAGES], v_empty[STAGES];
-  uint64_t s_full[2], p_full[2], pv_done[2], o_empty[2], drain;
+  uint64_t s_full[2], p_full[2], pv_done[2], o_empty[2], drain[2];
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -617,21 +617,22 @@ __global__ void __launch_bounds__(kThreads2, 1)
   const long long lim = p.wait_limit;
 
   if (threadIdx.x == 0) {
+    // stage and Q releases need both heads' MMAs: one commit from each issuer
     mbar_init(smem_u32(&sm.q_full), 1);
-    mbar_init(smem_u32(&sm.q_empty), 1);
+    mbar_init(smem_u32(&sm.q_empty), 2);
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(smem_u32(&sm.k_full[s]), 1);
-      mbar_init(smem_u32(&sm.k_empty[s]), 1);
+      mbar_init(smem_u32(&sm.k_empty[s]), 2);
       mbar_init(smem_u32(&sm.v_full[s]), 1);
-      mbar_init(smem_u32(&sm.v_empty[s]), 1);
+      mbar_init(smem_u32(&sm.v_empty[s]), 2);
     }
     for (int h = 0; h < 2; ++h) {
       mbar_init(smem_u32(&sm.s_full[h]), 1);
       mbar_init(smem_u32(&sm.p_full[h]), 128);
       mbar_init(smem_u32(&sm.pv_done[h]), 1);
       mbar_init(smem_u32(&sm.o_empty[h]), 128);
+      mbar_init(smem_u32(&sm.drain[h]), 1);
     }
-    mbar_init(smem_u32(&sm.drain), 1);
     sm.abort_flag = 0;
     fence_barrier_init();
   }
@@ -692,25 +693,29 @@ __global__ void __launch_bounds__(kThreads2, 1)
           }
       }
     }
-  } else if (warp == 1) {
-    // ============================================================ MMA issuer
+  } else if (warp == 1 || warp == 2) {
+    // ============================================================ MMA issuers: warp 1 for head 0, warp 2 for head 1
+    // Each head has its own issuing thread, so one head's MMAs never wait
+    // behind the other head's softmax.  tcgen05 operations of one thread run
+    // in issue order, which makes S_h(j+1) safe over the columns P.V_h(j) reads.
     if (lane == 0) {
-      uint32_t kv_cnt = 0, pf_cnt[2] = {0, 0};
+      const int h = warp - 1;
+      uint32_t kv_cnt = 0, pf_cnt = 0;
       bool ok = true;
       // descriptors of k-step 0; a k-step adds its byte offset / 16 to the start-address field
-      const uint64_t dq[2] = {desc_sw128(smem_u32(sm.q[0]), 16, 1024), desc_sw128(smem_u32(sm.q[1]), 16, 1024)};
+      const uint64_t dq = desc_sw128(smem_u32(sm.q[h]), 16, 1024);
       const uint64_t dk[STAGES] = {desc_sw128(smem_u32(sm.k[0]), 16, 1024), desc_sw128(smem_u32(sm.k[1]), 16, 1024)};
       const uint64_t dv[STAGES] = {desc_sw128(smem_u32(sm.v[0]), BN * 128, 1024),
                                    desc_sw128(smem_u32(sm.v[1]), BN * 128, 1024)};
-      auto issue_s = [&](int h, int st) {
+      auto issue_s = [&](int st) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off16 = ((kk >> 2) * (BM * 128) + (kk & 3) * 32) >> 4;
-          mma_bf16_ss(tmem + h * BN, dq[h] + off16, dk[st] + off16, kIdescS, kk > 0 ? 1u : 0u);
+          mma_bf16_ss(tmem + h * BN, dq + off16, dk[st] + off16, kIdescS, kk > 0 ? 1u : 0u);
         }
         mma_commit(smem_u32(&sm.s_full[h]));
       };
-      auto issue_pv = [&](int h, int st, bool first) {
+      auto issue_pv = [&](int st, bool first) {
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
           mma_bf16_ts(tmem + kColO + h * D, tmem + h * BN + kk * 8, dv[st] + ((kk * 16 * 128) >> 4), kIdescO,
@@ -722,13 +727,11 @@ __global__ void __launch_bounds__(kThreads2, 1)
         tile_of(p, it1, ti, qc, qi);
         const int nkv = n_kv_tiles(sch, qc, qi);
         if (!(ok = mbar_wait(smem_u32(&sm.q_full), ti & 1, abort_flag, lim, 110))) break;
-        // prologue: both score tiles of K/V tile 0
-        {
+        {  // scores of K/V tile 0
           const int st = kv_cnt % STAGES;
           if (!(ok = mbar_wait(smem_u32(&sm.k_full[st]), (kv_cnt / STAGES) & 1, abort_flag, lim, 111))) break;
           tc_fence_after();
-          issue_s(0, st);
-          issue_s(1, st);
+          issue_s(st);
           mma_commit(smem_u32(&sm.k_empty[st]));
           if (nkv == 1) mma_commit(smem_u32(&sm.q_empty));
         }
@@ -739,36 +742,28 @@ __global__ void __launch_bounds__(kThreads2, 1)
           const bool more = j + 1 < nkv;
           const int st1 = (c + 1) % STAGES;
           const uint32_t ph1 = ((c + 1) / STAGES) & 1;
-          // O_0 += P_0 V_j
-          if (!(ok = mbar_wait(smem_u32(&sm.p_full[0]), pf_cnt[0] & 1, abort_flag, lim, 112))) break;
-          ++pf_cnt[0];
-          if (!(ok = mbar_wait(smem_u32(&sm.v_full[st]), ph, abort_flag, lim, 113))) break;
-          if (j == 0 && !(ok = mbar_wait(smem_u32(&sm.o_empty[0]), (ti & 1) ^ 1, abort_flag, lim, 114))) break;
+          // O_h += P_h V_j
+          if (!(ok = mbar_wait(smem_u32(&sm.p_full[h]), pf_cnt & 1, abort_flag, lim, 112 + 4 * h))) break;
+          ++pf_cnt;
+          if (!(ok = mbar_wait(smem_u32(&sm.v_full[st]), ph, abort_flag, lim, 113 + 4 * h))) break;
+          if (j == 0 && !(ok = mbar_wait(smem_u32(&sm.o_empty[h]), (ti & 1) ^ 1, abort_flag, lim, 114 + 4 * h))) break;
           tc_fence_after();
-          issue_pv(0, st, j == 0);
-          // S_0 of tile j+1
-          if (more) {
-            if (!(ok = mbar_wait(smem_u32(&sm.k_full[st1]), ph1, abort_flag, lim, 115))) break;
-            tc_fence_after();
-            issue_s(0, st1);
-          }
-          // O_1 += P_1 V_j
-          if (!(ok = mbar_wait(smem_u32(&sm.p_full[1]), pf_cnt[1] & 1, abort_flag, lim, 116))) break;
-          ++pf_cnt[1];
-          if (j == 0 && !(ok = mbar_wait(smem_u32(&sm.o_empty[1]), (ti & 1) ^ 1, abort_flag, lim, 117))) break;
-          tc_fence_after();
-          issue_pv(1, st, j == 0);
+          issue_pv(st, j == 0);
           mma_commit(smem_u32(&sm.v_empty[st]));
+          // S_h of tile j+1
           if (more) {
-            issue_s(1, st1);
+            if (!(ok = mbar_wait(smem_u32(&sm.k_full[st1]), ph1, abort_flag, lim, 115 + 4 * h))) break;
+            tc_fence_after();
+            issue_s(st1);
             mma_commit(smem_u32(&sm.k_empty[st1]));
             if (j + 1 == nkv - 1) mma_commit(smem_u32(&sm.q_empty));
           }
         }
         kv_cnt += nkv;
       }
-      mma_commit(smem_u32(&sm.drain));
-      mbar_wait(smem_u32(&sm.drain), 0, abort_flag, ok ? lim : (1 << 22), 118);
+      // make sure none of this thread's MMAs still writes tensor memory before it is freed
+      mma_commit(smem_u32(&sm.drain[h]));
+      mbar_wait(smem_u32(&sm.drain[h]), 0, abort_flag, ok ? lim : (1 << 22), 118 + h);
     }
   } else if (warp >= 4) {
     // ============================================================ softmax + epilogue (head h)
@@ -858,292 +853,6 @@ __global__ void __launch_bounds__(kThreads2, 1)
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-// ===========================================================================
-// Variant 3: two GQA heads per CTA with 64-key K/V tiles and double-buffered
-// score tiles.  Tensor memory: S[h][b] = cols [64*(2h+b), +64) for head h and
-// buffer b, O[h] = cols [256 + D*h, +D).  P[h][b] (bf16 pairs) overwrites the
-// first 32 columns of S[h][b] and feeds P.V from tensor memory.  Because every
-// head has two score buffers, the MMA thread issues the scores of K/V tile j+2
-// as soon as P.V of tile j has been issued (same buffer, in-order execution),
-// so the tensor core always holds queued work while a softmax round trip is in
-// flight.  Issue order per tile j: PV0_j, PV1_j, S0_{j+2}, S1_{j+2}.
-// Shared memory: Q of both heads, a four-stage ring of 64-row K and V tiles.
-// ===========================================================================
-constexpr int BN3 = 64;
-constexpr int STAGES3 = 4;
-constexpr int kThreads3 = 384;
-
-template <int D>
-struct __align__(1024) Smem3 {
-  uint8_t q[2][BM * D * 2];
-  uint8_t k[STAGES3][BN3 * D * 2];
-  uint8_t v[STAGES3][BN3 * D * 2];
-  uint64_t q_full, q_empty, k_full[STAGES3], k_empty[STAGES3], v_full[STAGES3], v_empty[STAGES3];
-  uint64_t s_full[2][2], p_full[2][2], pv_done[2], o_full[2], o_empty[2], drain;
-  uint32_t tmem_base;
-  int abort_flag;
-};
-
-template <int D>
-__global__ void __launch_bounds__(kThreads3, 1)
-    ring_attn_bf16_pair64_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                                 const __grid_constant__ CUtensorMap tmV, const Params p) {
-  constexpr int SLABS = D / 64;
-  constexpr uint32_t kQBytes = BM * D * 2;
-  constexpr uint32_t kKVBytes = BN3 * D * 2;
-  constexpr uint32_t kIdescS = idesc_bf16_f32(BM, BN3, 0, 0);
-  constexpr uint32_t kIdescO = idesc_bf16_f32(BM, D, 0, 1);
-  constexpr uint32_t kColO3 = 4 * BN3;
-
-  extern __shared__ uint8_t smem_raw[];
-  Smem3<D>& sm = *reinterpret_cast<Smem3<D>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const Item2 it = decode_item2(p, blockIdx.x);
-  const Item it1{it.b, it.hq0, it.g, it.r, it.j};
-  const Sched sch{p.N, p.c, p.nt, p.causal, BN3, static_cast<int>((p.c + BN3 - 1) / BN3)};
-  volatile int* abort_flag = &sm.abort_flag;
-  const long long lim = p.wait_limit;
-
-  if (threadIdx.x == 0) {
-    mbar_init(smem_u32(&sm.q_full), 1);
-    mbar_init(smem_u32(&sm.q_empty), 1);
-    for (int s = 0; s < STAGES3; ++s) {
-      mbar_init(smem_u32(&sm.k_full[s]), 1);
-      mbar_init(smem_u32(&sm.k_empty[s]), 1);
-      mbar_init(smem_u32(&sm.v_full[s]), 1);
-      mbar_init(smem_u32(&sm.v_empty[s]), 1);
-    }
-    for (int h = 0; h < 2; ++h) {
-      for (int b = 0; b < 2; ++b) {
-        mbar_init(smem_u32(&sm.s_full[h][b]), 1);
-        mbar_init(smem_u32(&sm.p_full[h][b]), 128);
-      }
-      mbar_init(smem_u32(&sm.pv_done[h]), 1);
-      mbar_init(smem_u32(&sm.o_full[h]), 1);
-      mbar_init(smem_u32(&sm.o_empty[h]), 128);
-    }
-    mbar_init(smem_u32(&sm.drain), 1);
-    sm.abort_flag = 0;
-    fence_barrier_init();
-  }
-  if (warp == 1) {
-    tmem_alloc(smem_u32(&sm.tmem_base), kTmemCols);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = sm.tmem_base;
-
-  if (warp == 0) {
-    // ============================================================ TMA producer
-    if (lane == 0) {
-      tma_prefetch_desc(&tmQ);
-      tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmV);
-      uint32_t kv_cnt = 0;
-      bool ok = true;
-      for (int ti = 0; ti < 2 && ok; ++ti) {
-        int qc, qi;
-        tile_of(p, it1, ti, qc, qi);
-        if (!(ok = mbar_wait(smem_u32(&sm.q_empty), (ti & 1) ^ 1, abort_flag, lim, 201))) break;
-        const uint32_t qb = smem_u32(&sm.q_full);
-        mbar_arrive_expect_tx(qb, 2 * kQBytes);
-        const int32_t qrow = static_cast<int32_t>(token_row(p, it.b, qc, qi * BM));
-        for (int h = 0; h < 2; ++h)
-          for (int s = 0; s < SLABS; ++s)
-            tma_load_3d(smem_u32(sm.q[h] + s * BM * 128), &tmQ, qb, 64 * s, it.hq0 + h, qrow);
-        KvIter kv;
-        kv.init(sch, qc, qi);
-        int kc, kt;
-        while (kv.next(kc, kt)) {
-          const int st = kv_cnt % STAGES3;
-          const uint32_t ph = (kv_cnt / STAGES3) & 1;
-          const int32_t krow = static_cast<int32_t>(token_row(p, it.b, kc, kt * BN3));
-          if (!(ok = mbar_wait(smem_u32(&sm.k_empty[st]), ph ^ 1, abort_flag, lim, 202))) break;
-          mbar_arrive_expect_tx(smem_u32(&sm.k_full[st]), kKVBytes);
-          for (int s = 0; s < SLABS; ++s)
-            tma_load_3d(smem_u32(sm.k[st] + s * BN3 * 128), &tmK, smem_u32(&sm.k_full[st]), 64 * s, it.g, krow);
-          if (!(ok = mbar_wait(smem_u32(&sm.v_empty[st]), ph ^ 1, abort_flag, lim, 203))) break;
-          mbar_arrive_expect_tx(smem_u32(&sm.v_full[st]), kKVBytes);
-          for (int s = 0; s < SLABS; ++s)
-            tma_load_3d(smem_u32(sm.v[st] + s * BN3 * 128), &tmV, smem_u32(&sm.v_full[st]), 64 * s, it.g, krow);
-          ++kv_cnt;
-        }
-      }
-      if (!ok) {
-        // let the copies already in flight land before the CTA exits
-        for (int back = 1; back <= STAGES3 && back <= static_cast<int>(kv_cnt); ++back) {
-          const uint32_t c = kv_cnt - back;
-          mbar_wait(smem_u32(&sm.k_full[c % STAGES3]), (c / STAGES3) & 1, abort_flag, 1 << 22, 0);
-          mbar_wait(smem_u32(&sm.v_full[c % STAGES3]), (c / STAGES3) & 1, abort_flag, 1 << 22, 0);
-        }
-      }
-    }
-  } else if (warp == 1) {
-    // ============================================================ MMA issuer
-    if (lane == 0) {
-      uint32_t kv_cnt = 0;
-      bool ok = true;
-      const uint64_t dq[2] = {desc_sw128(smem_u32(sm.q[0]), 16, 1024), desc_sw128(smem_u32(sm.q[1]), 16, 1024)};
-      uint64_t dk[STAGES3], dv[STAGES3];
-      for (int s = 0; s < STAGES3; ++s) {
-        dk[s] = desc_sw128(smem_u32(sm.k[s]), 16, 1024);
-        dv[s] = desc_sw128(smem_u32(sm.v[s]), BN3 * 128, 1024);
-      }
-      // S[h][b] = Q_h K^T of the tile in stage st
-      auto issue_s = [&](int h, int st, int b) {
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_bf16_ss(tmem + (2 * h + b) * BN3, dq[h] + ((((kk >> 2) * (BM * 128)) + (kk & 3) * 32) >> 4),
-                      dk[st] + ((((kk >> 2) * (BN3 * 128)) + (kk & 3) * 32) >> 4), kIdescS, kk > 0 ? 1u : 0u);
-        mma_commit(smem_u32(&sm.s_full[h][b]));
-      };
-      // O_h += P[h][b] V of the tile in stage st
-      auto issue_pv = [&](int h, int st, int b, bool first) {
-#pragma unroll
-        for (int kk = 0; kk < BN3 / 16; ++kk)
-          mma_bf16_ts(tmem + kColO3 + h * D, tmem + (2 * h + b) * BN3 + kk * 8, dv[st] + ((kk * 16 * 128) >> 4),
-                      kIdescO, (kk > 0 || !first) ? 1u : 0u);
-        mma_commit(smem_u32(&sm.pv_done[h]));
-      };
-      for (int ti = 0; ti < 2 && ok; ++ti) {
-        int qc, qi;
-        tile_of(p, it1, ti, qc, qi);
-        const int nkv = n_kv_tiles(sch, qc, qi);
-        if (!(ok = mbar_wait(smem_u32(&sm.q_full), ti & 1, abort_flag, lim, 210))) break;
-        for (int jj = 0; jj < 2 && jj < nkv && ok; ++jj) {   // scores of the first two tiles
-          const uint32_t g = kv_cnt + jj;
-          const int st = g % STAGES3;
-          if (!(ok = mbar_wait(smem_u32(&sm.k_full[st]), (g / STAGES3) & 1, abort_flag, lim, 211))) break;
-          tc_fence_after();
-          issue_s(0, st, g & 1);
-          issue_s(1, st, g & 1);
-          mma_commit(smem_u32(&sm.k_empty[st]));
-          if (jj == nkv - 1) mma_commit(smem_u32(&sm.q_empty));
-        }
-        for (int j = 0; j < nkv && ok; ++j) {
-          const uint32_t g = kv_cnt + j;
-          const int st = g % STAGES3, b = g & 1;
-          const uint32_t ph4 = (g / STAGES3) & 1, ph2 = (g >> 1) & 1;
-          if (!(ok = mbar_wait(smem_u32(&sm.p_full[0][b]), ph2, abort_flag, lim, 212))) break;
-          if (!(ok = mbar_wait(smem_u32(&sm.v_full[st]), ph4, abort_flag, lim, 213))) break;
-          if (j == 0 && !(ok = mbar_wait(smem_u32(&sm.o_empty[0]), (ti & 1) ^ 1, abort_flag, lim, 214))) break;
-          tc_fence_after();
-          issue_pv(0, st, b, j == 0);
-          if (j == nkv - 1) mma_commit(smem_u32(&sm.o_full[0]));
-          if (!(ok = mbar_wait(smem_u32(&sm.p_full[1][b]), ph2, abort_flag, lim, 215))) break;
-          if (j == 0 && !(ok = mbar_wait(smem_u32(&sm.o_empty[1]), (ti & 1) ^ 1, abort_flag, lim, 216))) break;
-          tc_fence_after();
-          issue_pv(1, st, b, j == 0);
-          if (j == nkv - 1) mma_commit(smem_u32(&sm.o_full[1]));
-          mma_commit(smem_u32(&sm.v_empty[st]));
-          if (j + 2 < nkv) {   // scores of tile j+2 into the buffer P.V_j just consumed
-            const uint32_t g2 = g + 2;
-            const int st2 = g2 % STAGES3;
-            if (!(ok = mbar_wait(smem_u32(&sm.k_full[st2]), (g2 / STAGES3) & 1, abort_flag, lim, 217))) break;
-            tc_fence_after();
-            issue_s(0, st2, b);
-            issue_s(1, st2, b);
-            mma_commit(smem_u32(&sm.k_empty[st2]));
-            if (j + 2 == nkv - 1) mma_commit(smem_u32(&sm.q_empty));
-          }
-        }
-        kv_cnt += nkv;
-      }
-      mma_commit(smem_u32(&sm.drain));
-      mbar_wait(smem_u32(&sm.drain), 0, abort_flag, ok ? lim : (1 << 22), 218);
-    }
-  } else if (warp >= 4) {
-    // ============================================================ softmax + epilogue (head h)
-    const int h = (warp - 4) >> 2;
-    const int quarter = warp & 3;
-    const int row = quarter * 32 + lane;
-    const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    const uint32_t colO = kColO3 + h * D;
-    const int hq = it.hq0 + h;
-    uint32_t cnt = 0, pv_base = 0;
-    bool ok = true;
-    for (int ti = 0; ti < 2 && ok; ++ti) {
-      int qc, qi;
-      tile_of(p, it1, ti, qc, qi);
-      const int q_valid = min(BM, p.c - qi * BM);
-      const int nkv = n_kv_tiles(sch, qc, qi);
-      KvIter kv;
-      kv.init(sch, qc, qi);
-      float m = -CUDART_INF_F, l = 0.f;
-      for (int j = 0; j < nkv; ++j, ++cnt) {
-        int kc = 0, kt = 0;
-        kv.next(kc, kt);
-        const int b = cnt & 1;
-        const uint32_t colS = (2 * h + b) * BN3;
-        if (!(ok = mbar_wait(smem_u32(&sm.s_full[h][b]), (cnt >> 1) & 1, abort_flag, lim, 220 + h))) break;
-        tc_fence_after();
-        int col_lim;
-        bool masked;
-        tile_mask(sch, qc, qi, kc, kt, row, col_lim, masked);
-        uint32_t pk[BN3 / 2];
-        const float alpha = softmax_row(t_lane + colS, j, masked, col_lim, p.scale_log2, m, l, pk);
-        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-          // O_h must hold P.V of every earlier tile before it is rescaled
-          if (!(ok = mbar_wait(smem_u32(&sm.pv_done[h]), (pv_base + j - 1) & 1, abort_flag, lim, 224 + h))) break;
-          tc_fence_after();
-#pragma unroll
-          for (int c4 = 0; c4 < D / 32; ++c4) {
-            uint32_t orr[32];
-            tmem_ld32(t_lane + colO + 32 * c4, orr);
-            tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
-            tmem_st32(t_lane + colO + 32 * c4, orr);
-          }
-        }
-        tmem_st32(t_lane + colS, pk);
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(smem_u32(&sm.p_full[h][b]));
-      }
-      if (!ok) break;
-      // ---------------------------------------------------------- epilogue
-      // o_full completes once per query tile, after its last P.V: the per-P.V
-      // barrier may lag two phases here (scores run two tiles ahead), so its
-      // parity cannot be used for this wait.
-      if (!(ok = mbar_wait(smem_u32(&sm.o_full[h]), ti & 1, abort_flag, lim, 226 + h))) break;
-      pv_base += nkv;
-      tc_fence_after();
-      const float inv_l = l > 0.f ? 1.f / l : 0.f;
-      const bool row_ok = row < q_valid;
-      const int64_t trow = token_row(p, it.b, qc, qi * BM + row);
-      __nv_bfloat16* orow = p.o + (trow * p.Hq + hq) * D;
-#pragma unroll
-      for (int c4 = 0; c4 < D / 32; ++c4) {
-        uint32_t orr[32];
-        tmem_ld32(t_lane + colO + 32 * c4, orr);
-        tmem_wait_ld();
-        if (row_ok) {
-#pragma unroll
-          for (int i = 0; i < 32; i += 8) {
-            uint4 pk4;
-            pk4.x = f2_bf16x2(__uint_as_float(orr[i]) * inv_l, __uint_as_float(orr[i + 1]) * inv_l);
-            pk4.y = f2_bf16x2(__uint_as_float(orr[i + 2]) * inv_l, __uint_as_float(orr[i + 3]) * inv_l);
-            pk4.z = f2_bf16x2(__uint_as_float(orr[i + 4]) * inv_l, __uint_as_float(orr[i + 5]) * inv_l);
-            pk4.w = f2_bf16x2(__uint_as_float(orr[i + 6]) * inv_l, __uint_as_float(orr[i + 7]) * inv_l);
-            *reinterpret_cast<uint4*>(orow + 32 * c4 + i) = pk4;
-          }
-        }
-      }
-      tc_fence_before();
-      mbar_arrive(smem_u32(&sm.o_empty[h]));
-      if (row_ok) p.lse[trow * p.Hq + hq] = l > 0.f ? (m + log2f(l)) * kLn2 : -CUDART_INF_F;
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
-}
-
 // Per-rank tile classification with the kernels' own iterator (for tests):
 // visited tiles that need no mask, visited tiles with a causal mask, skipped.
 __global__ void schedule_counts_kernel(Sched s, unsigned long long* counts) {
@@ -1212,18 +921,6 @@ ra_status launch_bf16(const void* q, const void* k, const void* v, const Params&
   if ((st = make_map(&mk, k, D, prm.Hkv, rows)) != RA_OK) return st;
   if ((st = make_map(&mv, v, D, prm.Hkv, rows)) != RA_OK) return st;
   const int64_t tiles = static_cast<int64_t>(prm.B) * prm.Hq * prm.N * prm.nt;  // mirrored tile pairs x heads
-  if (variant == 3) {
-    CUtensorMap mk64, mv64;
-    if ((st = make_map(&mk64, k, D, prm.Hkv, rows, BN3)) != RA_OK) return st;
-    if ((st = make_map(&mv64, v, D, prm.Hkv, rows, BN3)) != RA_OK) return st;
-    const size_t smem = sizeof(Smem3<D>) + 1024;
-    RA_CUDA_TRY(cudaFuncSetAttribute(ring_attn_bf16_pair64_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     static_cast<int>(smem)));
-    ring_attn_bf16_pair64_kernel<D><<<static_cast<unsigned>(tiles / 2), kThreads3, smem, stream>>>(mq, mk64, mv64,
-                                                                                                 prm);
-    RA_LAUNCH_CHECK("ring_attn_bf16_pair64_kernel");
-    return RA_OK;
-  }
   if (variant == 2) {
     const size_t smem = sizeof(Smem2<D>) + 1024;
     RA_CUDA_TRY(cudaFuncSetAttribute(ring_attn_bf16_pair_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1264,7 +961,7 @@ extern "C" ra_status ra_ring_attn_fwd_ex(const void* q, const void* k, const voi
                                          int32_t causal, int32_t n_ranks, float scale, ra_layout layout,
                                          int32_t variant, ra_stream stream) {
   ra::clear_error();
-  RA_REQUIRE(variant >= 0 && variant <= 3, "variant must be 0, 1, 2 or 3");
+  RA_REQUIRE(variant >= 0 && variant <= 2, "variant must be 0, 1 or 2");
   RA_REQUIRE(B >= 1 && Hq >= 1 && Hkv >= 1 && S >= 1, "B, Hq, Hkv, S must be >= 1");
   RA_REQUIRE(Hq % Hkv == 0, "Hq (%d) must be a multiple of Hkv (%d)", Hq, Hkv);
   RA_REQUIRE(n_ranks >= 1, "n_ranks must be >= 1 (got %d)", n_ranks);
@@ -1291,7 +988,7 @@ extern "C" ra_status ra_ring_attn_fwd_ex(const void* q, const void* k, const voi
   const int64_t items = static_cast<int64_t>(B) * Hkv * n_ranks * prm.nt * prm.group;
   RA_REQUIRE(items < (int64_t(1) << 31), "too many work items");
   if (variant == 0) variant = (prm.group % 2 == 0) ? 2 : 1;
-  RA_REQUIRE(variant == 1 || prm.group % 2 == 0, "the two-head variants need an even Hq/Hkv");
+  RA_REQUIRE(variant == 1 || prm.group % 2 == 0, "the two-head variant needs an even Hq/Hkv");
   if (d == 128) return launch_bf16<128>(q, k, v, prm, variant, stream);
   return launch_bf16<64>(q, k, v, prm, variant, stream);
 }

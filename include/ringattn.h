@@ -133,10 +133,8 @@ ra_status ra_ring_attn_fwd(const void* q, const void* k, const void* v, void* o,
  * 1 = one query head per CTA (mirrored pair of query tiles, 128-key tiles,
  *     P via shared memory);
  * 2 = two query heads of one GQA group per CTA sharing every 128-key K/V tile
- *     (needs an even Hq/Hkv; P stays in tensor memory);
- * 3 = like 2 with 64-key K/V tiles and double-buffered score tiles, so the
- *     tensor core computes the scores of tile j+2 while tile j's softmax runs.
- * The variant is ignored for RA_F32.  All variants agree to rounding. */
+ *     (needs an even Hq/Hkv; P stays in tensor memory).
+ * The variant is ignored for RA_F32.  Both variants agree to rounding. */
 ra_status ra_ring_attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse,
                               int32_t B, int32_t Hq, int32_t Hkv, int32_t S, int32_t d,
                               ra_dtype dt, int32_t causal, int32_t n_ranks, float scale,
@@ -153,8 +151,8 @@ ra_status ra_ring_attn_fwd_ex(const void* q, const void* k, const void* v, void*
 ra_status ra_ring_schedule_counts(int32_t S, int32_t n_ranks, int32_t causal, int64_t* counts,
                                   ra_stream stream);
 
-/* Same with the key-tile length of the kernel variant: 128 (variants 1, 2)
- * or 64 (variant 3).  Query tiles are always 128 rows. */
+/* Same with an explicit key-tile length (64 or 128; the attention kernels use
+ * 128).  Query tiles are always 128 rows. */
 ra_status ra_ring_schedule_counts_ex(int32_t S, int32_t n_ranks, int32_t causal, int32_t kv_tile,
                                      int64_t* counts, ra_stream stream);
 

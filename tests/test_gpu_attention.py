@@ -67,16 +67,16 @@ def test_fp32_ragged_and_gqa(ra, S, N, causal, Hq, Hkv, d):
     (2048, 4, 1, 2, 2, 64, False),
     (16, 8, 1, 2, 2, 128, True),       # chunks of 1 token
 ])
-@pytest.mark.parametrize("variant", [1, 2, 3])
+@pytest.mark.parametrize("variant", [1, 2])
 def test_bf16_parity_small(ra, S, N, B, Hq, Hkv, d, causal, variant):
-    if variant >= 2 and (Hq // Hkv) % 2:
+    if variant == 2 and (Hq // Hkv) % 2:
         Hq = 2 * Hq                       # the two-head kernel needs an even GQA group
     q, k, v, o, lse = _run(ra, 3, B, S, Hq, Hkv, d, N, causal, torch.bfloat16, variant=variant)
     O, L = _oracle_full(q, k, v, B, S, causal)
     assert_parity(o, O, lse, L, torch.bfloat16, "bf16 v%d S=%d N=%d" % (variant, S, N))
 
 
-@pytest.mark.parametrize("other", [2, 3])
+@pytest.mark.parametrize("other", [2])
 def test_bf16_variants_agree(ra, other):
     B, S, Hq, Hkv, d, N = 1, 2560, 8, 2, 128, 5
     _, _, _, o1, l1 = _run(ra, 6, B, S, Hq, Hkv, d, N, True, torch.bfloat16, variant=1)
