@@ -559,15 +559,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ===========================================================================
 // Two-head variant for GQA (Hq/Hkv even): a CTA runs two query heads that read
 // the same K/V head, so every K/V tile TMA brings in feeds two score tiles.
-// Roles (384 threads): warp 0 TMA, warp 1 TMEM allocation + MMA issue for head
-// 0, warp 2 MMA issue for head 1, warps 4..7 softmax of head 0, warps 8..11
-// softmax of head 1 (warp 3 idle).
+// Roles (384 threads): warp 0 TMA, warp 1 TMEM allocation + MMA issue, warps
+// 4..7 softmax of head 0, warps 8..11 softmax of head 1 (warps 2, 3 idle).
 // Tensor memory: S_h = cols [128h, 128h+128), O_h = cols [256+128h, ...).
 // P_h (bf16, two per column) overwrites the first 64 columns of S_h and is
 // the A operand of O_h += P_h V straight from tensor memory, so P never
-// touches shared memory.  Each head's issuer runs PV_h(j), S_h(j+1), ...
-// (tcgen05 operations of one thread execute in issue order, so S_h(j+1) may
-// overwrite the columns PV_h(j) reads).  A softmax warpgroup only waits for
+// touches shared memory.  One thread issues every MMA, in the order
+//   PV0_j, S0_{j+1}, PV1_j, S1_{j+1}
+// which staggers the two heads: each softmax warpgroup works while the tensor
+// core serves the other head (measured faster than one issuer per head).
+// tcgen05 operations of one thread execute in issue order, so S_h(j+1) may
+// overwrite the columns PV_h(j) reads.  A softmax warpgroup only waits for
 // the previous P.V when it must rescale O (lazy rescale, threshold 2^8).
 // ===========================================================================
 struct Item2 {
@@ -591,7 +593,7 @@ struct __align__(1024) Smem2 {
   uint8_t k[STAGES][BN * D * 2];
   uint8_t v[STAGES][BN * D * 2];
   uint64_t q_full, q_empty, k_full[STAGES], k_empty[STAGES], v_full[STAGES], v_empty[STAGES];
-  uint64_t s_full[2], p_full[2], pv_done[2], o_empty[2], drain[2];
+  uint64_t s_full[2], p_full[2], pv_done[2], o_empty[2], drain;
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -617,22 +619,21 @@ __global__ void __launch_bounds__(kThreads2, 1)
   const long long lim = p.wait_limit;
 
   if (threadIdx.x == 0) {
-    // stage and Q releases need both heads' MMAs: one commit from each issuer
     mbar_init(smem_u32(&sm.q_full), 1);
-    mbar_init(smem_u32(&sm.q_empty), 2);
+    mbar_init(smem_u32(&sm.q_empty), 1);
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(smem_u32(&sm.k_full[s]), 1);
-      mbar_init(smem_u32(&sm.k_empty[s]), 2);
+      mbar_init(smem_u32(&sm.k_empty[s]), 1);
       mbar_init(smem_u32(&sm.v_full[s]), 1);
-      mbar_init(smem_u32(&sm.v_empty[s]), 2);
+      mbar_init(smem_u32(&sm.v_empty[s]), 1);
     }
     for (int h = 0; h < 2; ++h) {
       mbar_init(smem_u32(&sm.s_full[h]), 1);
       mbar_init(smem_u32(&sm.p_full[h]), 128);
       mbar_init(smem_u32(&sm.pv_done[h]), 1);
       mbar_init(smem_u32(&sm.o_empty[h]), 128);
-      mbar_init(smem_u32(&sm.drain[h]), 1);
     }
+    mbar_init(smem_u32(&sm.drain), 1);
     sm.abort_flag = 0;
     fence_barrier_init();
   }
@@ -693,29 +694,25 @@ __global__ void __launch_bounds__(kThreads2, 1)
           }
       }
     }
-  } else if (warp == 1 || warp == 2) {
-    // ============================================================ MMA issuers: warp 1 for head 0, warp 2 for head 1
-    // Each head has its own issuing thread, so one head's MMAs never wait
-    // behind the other head's softmax.  tcgen05 operations of one thread run
-    // in issue order, which makes S_h(j+1) safe over the columns P.V_h(j) reads.
+  } else if (warp == 1) {
+    // ============================================================ MMA issuer
     if (lane == 0) {
-      const int h = warp - 1;
-      uint32_t kv_cnt = 0, pf_cnt = 0;
+      uint32_t kv_cnt = 0, pf_cnt[2] = {0, 0};
       bool ok = true;
       // descriptors of k-step 0; a k-step adds its byte offset / 16 to the start-address field
-      const uint64_t dq = desc_sw128(smem_u32(sm.q[h]), 16, 1024);
+      const uint64_t dq[2] = {desc_sw128(smem_u32(sm.q[0]), 16, 1024), desc_sw128(smem_u32(sm.q[1]), 16, 1024)};
       const uint64_t dk[STAGES] = {desc_sw128(smem_u32(sm.k[0]), 16, 1024), desc_sw128(smem_u32(sm.k[1]), 16, 1024)};
       const uint64_t dv[STAGES] = {desc_sw128(smem_u32(sm.v[0]), BN * 128, 1024),
                                    desc_sw128(smem_u32(sm.v[1]), BN * 128, 1024)};
-      auto issue_s = [&](int st) {
+      auto issue_s = [&](int h, int st) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off16 = ((kk >> 2) * (BM * 128) + (kk & 3) * 32) >> 4;
-          mma_bf16_ss(tmem + h * BN, dq + off16, dk[st] + off16, kIdescS, kk > 0 ? 1u : 0u);
+          mma_bf16_ss(tmem + h * BN, dq[h] + off16, dk[st] + off16, kIdescS, kk > 0 ? 1u : 0u);
         }
         mma_commit(smem_u32(&sm.s_full[h]));
       };
-      auto issue_pv = [&](int st, bool first) {
+      auto issue_pv = [&](int h, int st, bool first) {
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
           mma_bf16_ts(tmem + kColO + h * D, tmem + h * BN + kk * 8, dv[st] + ((kk * 16 * 128) >> 4), kIdescO,
@@ -727,11 +724,13 @@ __global__ void __launch_bounds__(kThreads2, 1)
         tile_of(p, it1, ti, qc, qi);
         const int nkv = n_kv_tiles(sch, qc, qi);
         if (!(ok = mbar_wait(smem_u32(&sm.q_full), ti & 1, abort_flag, lim, 110))) break;
-        {  // scores of K/V tile 0
+        // prologue: both score tiles of K/V tile 0
+        {
           const int st = kv_cnt % STAGES;
           if (!(ok = mbar_wait(smem_u32(&sm.k_full[st]), (kv_cnt / STAGES) & 1, abort_flag, lim, 111))) break;
           tc_fence_after();
-          issue_s(st);
+          issue_s(0, st);
+          issue_s(1, st);
           mma_commit(smem_u32(&sm.k_empty[st]));
           if (nkv == 1) mma_commit(smem_u32(&sm.q_empty));
         }
@@ -742,28 +741,36 @@ __global__ void __launch_bounds__(kThreads2, 1)
           const bool more = j + 1 < nkv;
           const int st1 = (c + 1) % STAGES;
           const uint32_t ph1 = ((c + 1) / STAGES) & 1;
-          // O_h += P_h V_j
-          if (!(ok = mbar_wait(smem_u32(&sm.p_full[h]), pf_cnt & 1, abort_flag, lim, 112 + 4 * h))) break;
-          ++pf_cnt;
-          if (!(ok = mbar_wait(smem_u32(&sm.v_full[st]), ph, abort_flag, lim, 113 + 4 * h))) break;
-          if (j == 0 && !(ok = mbar_wait(smem_u32(&sm.o_empty[h]), (ti & 1) ^ 1, abort_flag, lim, 114 + 4 * h))) break;
+          // O_0 += P_0 V_j
+          if (!(ok = mbar_wait(smem_u32(&sm.p_full[0]), pf_cnt[0] & 1, abort_flag, lim, 112))) break;
+          ++pf_cnt[0];
+          if (!(ok = mbar_wait(smem_u32(&sm.v_full[st]), ph, abort_flag, lim, 113))) break;
+          if (j == 0 && !(ok = mbar_wait(smem_u32(&sm.o_empty[0]), (ti & 1) ^ 1, abort_flag, lim, 114))) break;
           tc_fence_after();
-          issue_pv(st, j == 0);
-          mma_commit(smem_u32(&sm.v_empty[st]));
-          // S_h of tile j+1
+          issue_pv(0, st, j == 0);
+          // S_0 of tile j+1
           if (more) {
-            if (!(ok = mbar_wait(smem_u32(&sm.k_full[st1]), ph1, abort_flag, lim, 115 + 4 * h))) break;
+            if (!(ok = mbar_wait(smem_u32(&sm.k_full[st1]), ph1, abort_flag, lim, 115))) break;
             tc_fence_after();
-            issue_s(st1);
+            issue_s(0, st1);
+          }
+          // O_1 += P_1 V_j
+          if (!(ok = mbar_wait(smem_u32(&sm.p_full[1]), pf_cnt[1] & 1, abort_flag, lim, 116))) break;
+          ++pf_cnt[1];
+          if (j == 0 && !(ok = mbar_wait(smem_u32(&sm.o_empty[1]), (ti & 1) ^ 1, abort_flag, lim, 117))) break;
+          tc_fence_after();
+          issue_pv(1, st, j == 0);
+          mma_commit(smem_u32(&sm.v_empty[st]));
+          if (more) {
+            issue_s(1, st1);
             mma_commit(smem_u32(&sm.k_empty[st1]));
             if (j + 1 == nkv - 1) mma_commit(smem_u32(&sm.q_empty));
           }
         }
         kv_cnt += nkv;
       }
-      // make sure none of this thread's MMAs still writes tensor memory before it is freed
-      mma_commit(smem_u32(&sm.drain[h]));
-      mbar_wait(smem_u32(&sm.drain[h]), 0, abort_flag, ok ? lim : (1 << 22), 118 + h);
+      mma_commit(smem_u32(&sm.drain));
+      mbar_wait(smem_u32(&sm.drain), 0, abort_flag, ok ? lim : (1 << 22), 118);
     }
   } else if (warp >= 4) {
     // ============================================================ softmax + epilogue (head h)
