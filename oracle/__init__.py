@@ -33,15 +33,16 @@ by the ``-m "not gpu"`` tests (closed forms, hand-worked golden values,
 invariants and brute force on tiny inputs).
 """
 
-from .attention import (full_attention, attention_rows, ring_attention,
-                        ring_partials, lse_merge, rank_chunks,
+from .attention import (full_attention, attention_rows, attention_block, segmented_attention,
+                        ring_attention, ring_partials, lse_merge, rank_chunks,
                         causal_pairs_per_rank, causal_tiles_per_rank)
 from .partition import zigzag_partition, gather_rows
 from .kvcache import (cp_slot_mapping, cp_token_location, cp_kv_scatter,
                       cp_decode, cp_decode_partials, decode_reference)
 
 __all__ = [
-    "full_attention", "attention_rows", "ring_attention", "ring_partials",
+    "full_attention", "attention_rows", "attention_block", "segmented_attention",
+    "ring_attention", "ring_partials",
     "lse_merge", "rank_chunks", "causal_pairs_per_rank", "causal_tiles_per_rank",
     "zigzag_partition", "gather_rows", "cp_slot_mapping", "cp_token_location",
     "cp_kv_scatter", "cp_decode", "cp_decode_partials", "decode_reference",

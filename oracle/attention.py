@@ -81,6 +81,44 @@ def attention_rows(q_rows, q_pos, k, v, causal: bool, scale=None):
     return O, LSE
 
 
+def attention_block(q_rows, q_pos0: int, k, v, k_pos0: int, causal: bool, scale=None):
+    """Partial attention of a query block against a key block.
+
+    Queries q_rows[i] sit at positions q_pos0 + i, keys/values k[j], v[j] at
+    k_pos0 + j.  Returns (O [n, Hq, d], LSE [n, Hq]) of softmax over the visible
+    keys of this block only; a row that sees none gets O = 0 and LSE = -inf.
+    These are the partials that the merge combines.
+    """
+    q_rows, k, v = _as64(q_rows), _as64(k), _as64(v)
+    n, Hq, d = q_rows.shape
+    sc = _default_scale(d, scale)
+    g_of = _kv_head_of(Hq, k.shape[1])
+    state = (np.full((n, Hq), NEG_INF), np.zeros((n, Hq)), np.zeros((n, Hq, d)))
+    qpos = q_pos0 + np.arange(n)
+    kpos = k_pos0 + np.arange(len(k))
+    state = _block_update(state, q_rows, qpos, k, v, kpos, causal, sc, g_of)
+    return _finish(state)
+
+
+def segmented_attention(q_rows, q_pos0: int, k, v, causal: bool, seg: int, scale=None):
+    """Chunked prefill with a bounded key segment per round (vLLM-Ascend
+    "Context Parallel (CP)", chunked prefill: a maximum amount of KV per round,
+    attention and online-softmax update segment after segment).
+
+    Keys 0..len(k)-1 are cut into segments of `seg` tokens; every segment gives
+    a partial (O, LSE) of the query block, and the partials are merged.
+    Returns (O, LSE, O_parts, LSE_parts).
+    """
+    parts_o, parts_l = [], []
+    for k0 in range(0, len(k), seg):
+        o, l = attention_block(q_rows, q_pos0, k[k0:k0 + seg], v[k0:k0 + seg], k0, causal, scale)
+        parts_o.append(o)
+        parts_l.append(l)
+    Op, Lp = np.stack(parts_o), np.stack(parts_l)
+    O, L = lse_merge(Op, Lp)
+    return O, L, Op, Lp
+
+
 def full_attention(q, k, v, causal: bool, scale=None, row_block: int = 1024):
     """Full softmax attention of one sequence (plain definition, float64).
 

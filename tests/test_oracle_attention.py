@@ -296,3 +296,30 @@ def test_causal_tiles_ragged_totals():
         assert full + part + skip == 2 * nt * 2 * N * nt
     # every visible pair is covered by a full or partial tile exactly once
     assert sum(oracle.causal_pairs_per_rank(N, c)) == (2 * N * c) * (2 * N * c + 1) // 2
+
+
+# ---------------------------------------------------------------- blocks and segmented prefill
+
+@pytest.mark.parametrize("seg", [1, 7, 64, 1000])
+@pytest.mark.parametrize("causal", [False, True])
+def test_segmented_attention_equals_plain_rows(seg, causal):
+    """A chunk of queries at positions 90..129 over keys 0..129, any segment length:
+    merging the segment partials gives the plain attention of those rows."""
+    rng = np.random.default_rng(40 + seg)
+    q, k, v = _rand(rng, 130, 4, 2, 8)
+    rows = np.arange(90, 130)
+    O, L, Op, Lp = oracle.segmented_attention(q[rows], 90, k, v, causal, seg)
+    Or, Lr = oracle.attention_rows(q[rows], rows, k, v, causal)
+    np.testing.assert_allclose(O, Or, atol=1e-12)
+    np.testing.assert_allclose(L, Lr, atol=1e-12)
+    assert Op.shape[0] == -(-130 // seg)
+
+
+def test_attention_block_rows_before_every_key_are_empty():
+    rng = np.random.default_rng(41)
+    q, k, v = _rand(rng, 12, 2, 1, 4)
+    # queries at 0..5, keys at 3..14: rows 0..2 see nothing, row 3 sees key 3 only
+    O, L = oracle.attention_block(q[:6], 0, k, v, 3, True)
+    assert np.all(np.isneginf(L[:3])) and np.all(O[:3] == 0)
+    np.testing.assert_allclose(O[3], v[0, [0, 0]], atol=1e-15)
+    np.testing.assert_allclose(L[3], 0.5 * np.einsum("hd,hd->h", q[3], k[0, [0, 0]]), atol=1e-14)
