@@ -325,6 +325,7 @@ def run_ours(args, rank, world, dev):
         "gpu_launches": wl.launches_per_step * args.steps,
         "clocks": clk.summary(),
     }
+    line["next_segmented_prefill"] = measure_segmented(ra, dev)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_rows)
     return line
@@ -353,6 +354,36 @@ def run_parts(args, dev):
     if "decode" in parts:
         out["decode_merge_gbs"] = wl.decode_bytes()[0] / (out["decode_merge_ms"] * 1e-3) / 1e9
     print(json.dumps(out), flush=True)
+
+
+SEGMENTED = dict(ctx=122880, Tq=8192, Hq=32, Hkv=8, d=128, seg=32768, seed=6)
+
+
+def measure_segmented(ra, dev, reps=5):
+    """Chunked prefill with bounded KV per round (the next scope row): Tq new tokens after ctx cached
+    ones, key segments of `seg` tokens, partials merged by LSE.  Timed alone with CUDA events."""
+    S = SEGMENTED
+    T = S["ctx"] + S["Tq"]
+    tab = I.normal_table(torch.bfloat16)
+    q = ra.synth_fill(I.tensor_key(S["seed"], I.TID_Q), tab, (S["Tq"], S["Hq"], S["d"]), dev)
+    k = ra.synth_fill(I.tensor_key(S["seed"], I.TID_K), tab, (T, S["Hkv"], S["d"]), dev)
+    v = ra.synth_fill(I.tensor_key(S["seed"], I.TID_V), tab, (T, S["Hkv"], S["d"]), dev)
+    for _ in range(2):
+        ra.segmented_prefill_fwd(q, k, v, S["ctx"], S["seg"])
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        ra.segmented_prefill_fwd(q, k, v, S["ctx"], S["seg"])
+    e1.record()
+    torch.cuda.synchronize()
+    if ra.device_status() != 0:
+        raise RuntimeError("device status after the segmented prefill: %s" % ra.last_error())
+    ms = e0.elapsed_time(e1) / reps
+    pairs = sum(range(S["ctx"] + 1, T + 1))          # query at position i sees i+1 keys
+    flops = 4.0 * S["Hq"] * S["d"] * pairs
+    return {"config": S, "ms": round(ms, 3), "tflops": round(flops / (ms * 1e-3) / 1e12, 1),
+            "frac_of_bf16_sustained": round(flops / (ms * 1e-3) / 1e12 / _peaks()["bf16_sus"], 4)}
 
 
 # ---------------------------------------------------------------------------- oracle arm

@@ -35,6 +35,10 @@ SIGNATURES = {
     "ra_ring_schedule_counts": [_i32, _i32, _i32, _vp, _vp],
     "ra_ring_schedule_counts_ex": [_i32, _i32, _i32, _i32, _vp, _vp],
     "ra_lse_merge": [_vp, _vp, _i32, _i64, _i32, _i32, _vp, _c.c_int, _vp, _vp],
+    "ra_attn_block_fwd": [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i64, _i64, _i32, _f32, _vp, _vp, _vp],
+    "ra_segmented_prefill_workspace_size": [_i32, _i32, _i32, _i32, _i32, _c.POINTER(_sz)],
+    "ra_segmented_prefill_fwd": [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i64, _i32, _f32, _i32, _vp,
+                                 _c.c_int, _vp, _vp, _sz, _vp],
     "ra_cp_slot_mapping": [_vp, _vp, _vp, _i32, _i32, _i64, _i32, _i32, _i32, _i32, _vp, _vp],
     "ra_cp_kv_scatter": [_vp, _vp, _vp, _vp, _vp, _i64, _i32, _i32, _i32, _i32, _i64, _c.c_int, _vp],
     "ra_cp_decode_workspace_size": [_i32, _i32, _i32, _i32, _i32, _i32, _i32, _c.POINTER(_sz)],
@@ -175,6 +179,44 @@ def ring_schedule_counts(S: int, n_ranks: int, causal: bool, kv_tile: int = 128,
     out = torch.empty((n_ranks, 3), dtype=torch.int64, device=device)
     _check(lib().ra_ring_schedule_counts_ex(S, n_ranks, 1 if causal else 0, kv_tile, _ptr(out), _stream()))
     return out
+
+
+def attn_block_fwd(q, k, v, q_pos0: int, k_pos0: int, causal: bool, scale: Optional[float] = None,
+                   o_part=None, lse_part=None):
+    """Partial attention of q [Tq, Hq, d] (positions q_pos0..) over k/v [Tk, Hkv, d] (positions k_pos0..)
+    -> (O_part fp32 [Tq, Hq, d], LSE_part [Tq, Hq]); -inf / 0 for rows with no visible key."""
+    _need_cuda(q, k, v, o_part, lse_part)
+    Tq, Hq, d = q.shape
+    Tk, Hkv, _ = k.shape
+    if o_part is None:
+        o_part = torch.empty((Tq, Hq, d), dtype=torch.float32, device=q.device)
+    if lse_part is None:
+        lse_part = torch.empty((Tq, Hq), dtype=torch.float32, device=q.device)
+    _check(lib().ra_attn_block_fwd(_ptr(q), _ptr(k), _ptr(v), Tq, Tk, Hq, Hkv, d, int(q_pos0), int(k_pos0),
+                                   1 if causal else 0, float(scale or 0.0), _ptr(o_part), _ptr(lse_part),
+                                   _stream()))
+    return o_part, lse_part
+
+
+def segmented_prefill_fwd(q, k, v, q_pos0: int, seg_tokens: int, causal: bool = True,
+                          scale: Optional[float] = None, out_dtype=torch.bfloat16, workspace=None):
+    """Chunked prefill of q [Tq, Hq, d] (positions q_pos0..) over k/v [Tk, Hkv, d] (positions 0..) in
+    key segments of seg_tokens -> (O [Tq, Hq, d], LSE [Tq, Hq])."""
+    _need_cuda(q, k, v, workspace)
+    Tq, Hq, d = q.shape
+    Tk, Hkv, _ = k.shape
+    n = _sz(0)
+    _check(lib().ra_segmented_prefill_workspace_size(Tq, Tk, Hq, d, seg_tokens, _c.byref(n)))
+    if workspace is None:
+        workspace = torch.empty(n.value, dtype=torch.uint8, device=q.device)
+    o = torch.empty((Tq, Hq, d), dtype=out_dtype, device=q.device)
+    lse = torch.empty((Tq, Hq), dtype=torch.float32, device=q.device)
+    _check(lib().ra_segmented_prefill_fwd(_ptr(q), _ptr(k), _ptr(v), Tq, Tk, Hq, Hkv, d, int(q_pos0),
+                                          1 if causal else 0, float(scale or 0.0), seg_tokens, _ptr(o),
+                                          RA_BF16 if out_dtype == torch.bfloat16 else RA_F32, _ptr(lse),
+                                          _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                          _stream()))
+    return o, lse
 
 
 def lse_merge(o_parts, lse_parts, out_dtype=torch.float32):

@@ -157,6 +157,50 @@ ra_status ra_ring_schedule_counts_ex(int32_t S, int32_t n_ranks, int32_t causal,
                                      int64_t* counts, ra_stream stream);
 
 /* ------------------------------------------------------------------------
+ * ra_attn_block_fwd -- partial attention of one query block against one key
+ * block: the computation of one ring step (a rank's Q against the K/V block it
+ * holds) or of one segment of a chunked prefill, whose partials ra_lse_merge
+ * combines.  Sources: guijiagi.com "Ring Attention" tag page (per-step partial
+ * attention, blockwise decomposition); vLLM-Ascend "Context Parallel (CP)",
+ * chunked prefill (segments of bounded KV, online-softmax update per segment).
+ *
+ * q        device bf16 [Tq, Hq, d]: queries at positions q_pos0 .. q_pos0+Tq-1.
+ * k, v     device bf16 [Tk, Hkv, d]: keys at positions k_pos0 .. k_pos0+Tk-1.
+ * o_part   device float [Tq, Hq, d] out: softmax-weighted V over the visible keys
+ *          of this block (normalised by the block's own sum), 0 if none.
+ * lse_part device float [Tq, Hq] out: natural-log sum of exp(scaled scores)
+ *          over the visible keys, -inf if none.
+ * causal != 0: key position j is visible to query position i iff j <= i.
+ * Same GQA mapping, scale and d rules as ra_ring_attn_fwd; bf16 only.
+ * ---------------------------------------------------------------------- */
+ra_status ra_attn_block_fwd(const void* q, const void* k, const void* v, int32_t Tq, int32_t Tk,
+                            int32_t Hq, int32_t Hkv, int32_t d, int64_t q_pos0, int64_t k_pos0,
+                            int32_t causal, float scale, float* o_part, float* lse_part,
+                            ra_stream stream);
+
+/* ------------------------------------------------------------------------
+ * ra_segmented_prefill_fwd -- chunked prefill with a bounded KV segment per
+ * round (vLLM-Ascend "Context Parallel (CP)", chunked prefill, segmented
+ * AllGatherKV): the key range [0, Tk) is cut into segments of seg_tokens; each
+ * segment gives partials (ra_attn_block_fwd) and the partials are merged
+ * (ra_lse_merge).  The result equals attention of the query block over all
+ * Tk keys.
+ *
+ * q [Tq, Hq, d] at positions q_pos0..; k, v [Tk, Hkv, d] at positions 0..Tk-1
+ * (bf16, device).  o [Tq, Hq, d] out in out_dt; lse [Tq, Hq] fp32 out (may be
+ * NULL).  workspace: ra_segmented_prefill_workspace_size() bytes, 16-byte
+ * aligned (the per-segment fp32 partials).
+ * ---------------------------------------------------------------------- */
+ra_status ra_segmented_prefill_workspace_size(int32_t Tq, int32_t Tk, int32_t Hq, int32_t d,
+                                              int32_t seg_tokens, size_t* bytes);
+
+ra_status ra_segmented_prefill_fwd(const void* q, const void* k, const void* v, int32_t Tq,
+                                   int32_t Tk, int32_t Hq, int32_t Hkv, int32_t d, int64_t q_pos0,
+                                   int32_t causal, float scale, int32_t seg_tokens, void* o,
+                                   ra_dtype out_dt, float* lse, void* workspace, size_t ws_bytes,
+                                   ra_stream stream);
+
+/* ------------------------------------------------------------------------
  * ra_lse_merge -- merge P partial attention results (the update of a
  * cp_lse_ag_out_rs-style gather: vLLM-Ascend "Context Parallel (CP)", DCP
  * decode; weights from the blockwise decomposition of the "Ring Attention"

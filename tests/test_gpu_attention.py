@@ -164,6 +164,44 @@ def test_bf16_long_context_131k(ra):
     _check_sampled(o, lse, seed, 0, S, Hq, Hkv, d, np.unique(rows))
 
 
+# --------------------------------------------------------------------- block partials and segmented prefill
+
+@pytest.mark.parametrize("Tq,Tk,q0,k0,causal,Hq,Hkv,d", [
+    (300, 500, 400, 0, True, 4, 2, 128),      # ragged tiles, queries after part of the keys
+    (128, 256, 0, 100, True, 2, 2, 128),      # rows before every key: LSE -inf, O 0
+    (77, 1000, 5000, 0, True, 8, 2, 64),      # every key visible
+    (200, 333, 0, 0, False, 4, 1, 128),       # non-causal
+    (256, 128, 0, 300, True, 2, 1, 128),      # no key visible to any row of the block
+])
+def test_block_partial_matches_oracle(ra, Tq, Tk, q0, k0, causal, Hq, Hkv, d):
+    q = I.synth_normal(71, I.TID_Q, (Tq, Hq, d), torch.bfloat16)
+    k = I.synth_normal(71, I.TID_K, (Tk, Hkv, d), torch.bfloat16)
+    v = I.synth_normal(71, I.TID_V, (Tk, Hkv, d), torch.bfloat16)
+    o, lse = ra.attn_block_fwd(q.cuda(), k.cuda(), v.cuda(), q0, k0, causal)
+    check_status(ra)
+    O, L = oracle.attention_block(q, q0, k, v, k0, causal)
+    lg = lse.cpu().numpy()
+    assert np.array_equal(np.isneginf(lg), np.isneginf(L))
+    live = np.isfinite(L)
+    e = np.abs(o.cpu().numpy().astype(np.float64) - O)
+    assert e.max() <= 2e-2 and e.mean() <= 2e-3, (e.max(), e.mean())
+    assert np.abs(lg[live] - L[live]).max(initial=0) <= 1e-3
+
+
+@pytest.mark.parametrize("ctx,Tq,seg,Hq,Hkv", [(3000, 700, 1024, 4, 2), (513, 255, 128, 2, 1), (0, 600, 200, 4, 4)])
+def test_segmented_prefill_matches_full_attention(ra, ctx, Tq, seg, Hq, Hkv):
+    """A chunk of Tq new tokens after ctx cached ones attends causally to all ctx+Tq keys, in
+    segments of seg keys merged by LSE; equal to the plain attention rows."""
+    d, T = 128, ctx + Tq
+    q = I.synth_normal(72, I.TID_Q, (Tq, Hq, d), torch.bfloat16)
+    k = I.synth_normal(72, I.TID_K, (T, Hkv, d), torch.bfloat16)
+    v = I.synth_normal(72, I.TID_V, (T, Hkv, d), torch.bfloat16)
+    o, lse = ra.segmented_prefill_fwd(q.cuda(), k.cuda(), v.cuda(), ctx, seg)
+    check_status(ra)
+    O, L = oracle.attention_rows(q, np.arange(ctx, T), k, v, True)
+    assert_parity(o, O, lse, L, torch.bfloat16, "segmented prefill")
+
+
 # --------------------------------------------------------------------- schedule
 
 @pytest.mark.parametrize("S,N", [(512, 2), (640, 2), (8192, 8), (1200, 3), (16, 8), (2 * 16 * 300, 16)])
