@@ -36,7 +36,9 @@ from context_long_sequence_ring_gb300 import inputs as I  # noqa: E402
 METRIC = "ring-attn fwd TFLOP/s (causal-adj) & % bf16 peak; decode+merge GB/s % HBM"
 PREFILL = dict(B=1, Hq=32, Hkv=8, S=131072, d=128, N=16, seed=5)
 DECODE = dict(R=64, lo=4096, hi=131072, Hq=32, Hkv=8, d=128, bs=128, I=16, pcp=2, dcp=4, seed=4, split=8)
-KERNEL_SOURCES = {"ring_attn_bf16": "ra_attn_bf16.cu", "cp_decode": "ra_decode.cu"}
+# sources whose contents the recorded DRAM traffic of each kernel was measured on
+KERNEL_SOURCES = {"ring_attn_bf16": ["ra_attn_bf16.cu", "ra_attn_tc.cuh", "ra_sm100.cuh"],
+                  "cp_decode": ["ra_decode.cu"]}
 
 
 def causal_flops(B, Hq, S, d):
@@ -53,10 +55,12 @@ def _peaks():
         return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
 
 
-def _source_hash(name):
-    p = os.path.join(ROOT, "context_long_sequence_ring_gb300", "csrc", name)
-    with open(p, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+def _source_hash(names):
+    h = hashlib.sha256()
+    for name in names:
+        with open(os.path.join(ROOT, "context_long_sequence_ring_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def _traffic(kernel):

@@ -36,27 +36,13 @@
 // S_{j+1}.  O is rescaled in tensor memory only when a row's running max grows
 // by more than 2^8 (the stale max is exact as long as l and O use the same
 // reference and P stays in range).
-#include <cuda.h>
-#include <math_constants.h>
-
-#include <cstdlib>
-
-#include "ra_common.cuh"
-#include "ra_sm100.cuh"
+#include "ra_attn_tc.cuh"
 
 RA_DEFINE_ERROR_FETCH(fetch_error_attn_bf16)
 
 namespace {
 
 using namespace ra::sm100;
-
-constexpr int BM = 128;       // query rows per tile
-constexpr int BN = 128;       // keys per K/V tile
-constexpr int STAGES = 2;     // K/V shared-memory ring depth
-constexpr int kThreads = 192;
-constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS0 = 0, kColO = 2 * BN;
-constexpr float kLn2 = 0.6931471805599453f;
 
 // ------------------------------------------------------------------ schedule
 struct Sched {
@@ -142,161 +128,6 @@ __device__ __forceinline__ Item decode_item(const Params& p, int idx) {
 __device__ __forceinline__ void tile_of(const Params& p, const Item& it, int ti, int& qc, int& qi) {
   if (ti == 0) { qc = it.r; qi = it.j; }
   else { qc = 2 * p.N - 1 - it.r; qi = p.nt - 1 - it.j; }
-}
-
-template <int D>
-struct __align__(1024) Smem {
-  uint8_t q[BM * D * 2];
-  uint8_t k[STAGES][BN * D * 2];
-  uint8_t v[STAGES][BN * D * 2];
-  uint8_t p[BM * BN * 2];
-  uint64_t q_full, q_empty, k_full[STAGES], k_empty[STAGES], v_full[STAGES], v_empty[STAGES];
-  uint64_t s_full[2], s_empty[2], p_full, pv_done, o_empty, drain;
-  uint32_t tmem_base;
-  int abort_flag;
-};
-
-__device__ __forceinline__ uint32_t f2_bf16x2(float lo, float hi) {
-  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&h);
-}
-
-// 2^x with the SFU instruction (flush-to-zero; 2^-inf = 0).
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-// ------------------------------------------------------------------ softmax of one row
-__device__ __forceinline__ uint64_t f2pack(float a, float b) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
-  return r;
-}
-__device__ __forceinline__ void f2unpack(uint64_t r, float& a, float& b) {
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
-}
-__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-  return d;
-}
-__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
-  uint64_t d;
-  asm("add.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-__device__ __forceinline__ float fmax3(float a, float b, float c) {
-  float d;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-  return d;
-}
-
-// Columns [c0, c0+32) of a score row: mask (when asked) and return the max.
-__device__ __forceinline__ float chunk_mask_max(uint32_t (&x)[32], int c0, bool masked, int col_lim) {
-  if (masked) {
-#pragma unroll
-    for (int i = 0; i < 32; ++i)
-      if (c0 + i >= col_lim) x[i] = __float_as_uint(-CUDART_INF_F);
-  }
-  float mx[4];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) mx[k] = __uint_as_float(x[k]);
-#pragma unroll
-  for (int i = 4; i < 32; i += 8)
-#pragma unroll
-    for (int k = 0; k < 4; ++k) mx[k] = fmax3(mx[k], __uint_as_float(x[i + k]), __uint_as_float(x[i + 4 + k]));
-  return fmax3(fmax3(mx[0], mx[1], mx[2]), mx[3], mx[3]);
-}
-
-// p = 2^(s*scale - m_ref) for 32 columns, packed to bf16 pairs into pk[0..16); adds the
-// fp32 sums into two packed accumulators.
-__device__ __forceinline__ void chunk_exp_pack(const uint32_t (&x)[32], uint64_t sc2, uint64_t negm2,
-                                               uint64_t& acc0, uint64_t& acc1, uint32_t* pk) {
-#pragma unroll
-  for (int i = 0; i < 32; i += 2) {
-    float t0, t1;
-    f2unpack(ffma2(f2pack(__uint_as_float(x[i]), __uint_as_float(x[i + 1])), sc2, negm2), t0, t1);
-    const float p0 = ex2(t0), p1 = ex2(t1);
-    if ((i >> 1) & 1) acc1 = fadd2(acc1, f2pack(p0, p1)); else acc0 = fadd2(acc0, f2pack(p0, p1));
-    pk[i >> 1] = f2_bf16x2(p0, p1);
-  }
-}
-
-// One online-softmax step for the score row at tensor-memory address s_addr
-// (BN fp32 columns, raw Q.K^T): fills pk with P in bf16 pairs and updates the
-// running max m (log2 units) and sum l.  Returns the factor O must be scaled by
-// (1 when unchanged).
-//
-// After the first K/V tile the row is read once, 32 columns at a time, with the
-// running max as reference: the exps start before the whole row is seen.  If
-// any row of the warp finds a score above max + 8 (log2), the warp falls back
-// to two passes (max, then exps) and the rows that grew move their reference.
-// The stale reference is exact because l and O always share it; 2^8 bounds P.
-template <int NP>
-__device__ __forceinline__ float softmax_row(uint32_t s_addr, int j, bool masked, int col_lim, float scale,
-                                             float& m, float& l, uint32_t (&pk)[NP]) {
-  constexpr int NCOL = 2 * NP;
-  const uint64_t sc2 = f2pack(scale, scale);
-  if (j > 0) {
-    const float thr = (m + 8.f) / scale;   // raw-score threshold of a rescale
-    const uint64_t negm2 = f2pack(-m, -m);
-    uint64_t acc0 = f2pack(0.f, 0.f), acc1 = acc0;
-    bool grow = false;
-    // the load of chunk c+1 is in flight while chunk c is processed
-    uint32_t xa[32], xb[32];
-    tmem_ld32(s_addr, xa);
-    tmem_wait_ld();
-#pragma unroll
-    for (int c = 0; c < NCOL / 32; ++c) {
-      uint32_t (&x)[32] = (c & 1) ? xb : xa;
-      uint32_t (&y)[32] = (c & 1) ? xa : xb;
-      if (c + 1 < NCOL / 32) tmem_ld32(s_addr + 32 * (c + 1), y);
-      const float cm = chunk_mask_max(x, 32 * c, masked, col_lim);
-      if (__any_sync(0xffffffffu, cm > thr)) { grow = true; tmem_wait_ld(); break; }
-      chunk_exp_pack(x, sc2, negm2, acc0, acc1, &pk[16 * c]);
-      if (c + 1 < NCOL / 32) tmem_wait_ld();
-    }
-    if (!grow) {
-      float a0, a1, b0, b1;
-      f2unpack(acc0, a0, a1);
-      f2unpack(acc1, b0, b1);
-      l += (a0 + a1) + (b0 + b1);
-      return 1.f;
-    }
-  }
-  // two passes: the row max, then the exps against the (possibly new) reference
-  float mx = -CUDART_INF_F;
-#pragma unroll
-  for (int c = 0; c < NCOL / 32; ++c) {
-    uint32_t x[32];
-    tmem_ld32(s_addr + 32 * c, x);
-    tmem_wait_ld();
-    mx = fmaxf(mx, chunk_mask_max(x, 32 * c, masked, col_lim));
-  }
-  const float m_tile = mx * scale;
-  const bool need = (j == 0) || (m_tile > m + 8.f);
-  const float m_use = need ? fmaxf(m, m_tile) : m;
-  const float m_ref = (m_use == -CUDART_INF_F) ? 0.f : m_use;
-  const float alpha = (j == 0) ? 0.f : ex2(m - m_ref);
-  const uint64_t negm2 = f2pack(-m_ref, -m_ref);
-  uint64_t acc0 = f2pack(0.f, 0.f), acc1 = acc0;
-#pragma unroll
-  for (int c = 0; c < NCOL / 32; ++c) {
-    uint32_t x[32];
-    tmem_ld32(s_addr + 32 * c, x);
-    tmem_wait_ld();
-    chunk_mask_max(x, 32 * c, masked, col_lim);
-    chunk_exp_pack(x, sc2, negm2, acc0, acc1, &pk[16 * c]);
-  }
-  float a0, a1, b0, b1;
-  f2unpack(acc0, a0, a1);
-  f2unpack(acc1, b0, b1);
-  const float rs = (a0 + a1) + (b0 + b1);
-  l = (j == 0) ? rs : l * alpha + rs;
-  m = m_use;
-  return (j == 0) ? 1.f : alpha;
 }
 
 template <int D>
@@ -860,254 +691,6 @@ __global__ void __launch_bounds__(kThreads2, 1)
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-// ===========================================================================
-// Block partial attention: queries at positions q_pos0 + i against keys at
-// positions k_pos0 + j (one K/V block of a ring step, or one segment of a
-// chunked prefill), causal by absolute position.  Output: the partial's O
-// (fp32, already normalised by its own row sum) and LSE, to be combined with
-// other partials by the LSE merge.  One CTA per (128-row query tile, query
-// head); the pipeline is that of the one-head ring kernel (TMA producer, one
-// MMA thread, a softmax warpgroup, P via shared memory, double-buffered S).
-// A row with no visible key gets O = 0 and LSE = -inf.
-// ===========================================================================
-struct BlockParams {
-  int Tq, Tk, Hq, Hkv, group, causal;
-  long long q_pos0, k_pos0;
-  float scale_log2;
-  float* o;    // [Tq, Hq, D] fp32
-  float* lse;  // [Tq, Hq]
-  long long wait_limit;
-};
-
-// Key tiles [0, nk) a query tile meets (tiles of BN keys, the last may be short).
-__device__ __forceinline__ int block_n_kv(const BlockParams& p, int qt) {
-  const int ntk = (p.Tk + BN - 1) / BN;
-  if (!p.causal) return ntk;
-  const int q_valid = min(BM, p.Tq - qt * BM);
-  const long long last_q = p.q_pos0 + static_cast<long long>(qt) * BM + q_valid - 1;
-  if (last_q < p.k_pos0) return 0;
-  const long long seen = (last_q - p.k_pos0) / BN + 1;
-  return static_cast<int>(seen < ntk ? seen : ntk);
-}
-
-template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
-    block_attn_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                           const __grid_constant__ CUtensorMap tmV, const BlockParams p) {
-  constexpr int SLABS = D / 64;
-  constexpr uint32_t kTileBytes = BM * D * 2;
-  constexpr uint32_t kIdescS = idesc_bf16_f32(BM, BN, 0, 0);
-  constexpr uint32_t kIdescO = idesc_bf16_f32(BM, D, 0, 1);
-
-  extern __shared__ uint8_t smem_raw[];
-  Smem<D>& sm = *reinterpret_cast<Smem<D>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int hq = blockIdx.x % p.Hq, qt = blockIdx.x / p.Hq;
-  const int g = hq / p.group;
-  const int nkv = block_n_kv(p, qt);
-  const int q_valid = min(BM, p.Tq - qt * BM);
-  volatile int* abort_flag = &sm.abort_flag;
-  const long long lim = p.wait_limit;
-
-  if (nkv == 0) {  // every key of the block is after every query of the tile
-    for (int i = threadIdx.x; i < q_valid * D; i += blockDim.x) {
-      const int r = i / D, e = i % D;
-      p.o[(static_cast<int64_t>(qt * BM + r) * p.Hq + hq) * D + e] = 0.f;
-      if (e == 0) p.lse[static_cast<int64_t>(qt * BM + r) * p.Hq + hq] = -CUDART_INF_F;
-    }
-    return;
-  }
-
-  if (threadIdx.x == 0) {
-    mbar_init(smem_u32(&sm.q_full), 1);
-    mbar_init(smem_u32(&sm.q_empty), 1);
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(smem_u32(&sm.k_full[s]), 1);
-      mbar_init(smem_u32(&sm.k_empty[s]), 1);
-      mbar_init(smem_u32(&sm.v_full[s]), 1);
-      mbar_init(smem_u32(&sm.v_empty[s]), 1);
-    }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(smem_u32(&sm.s_full[s]), 1);
-      mbar_init(smem_u32(&sm.s_empty[s]), 128);
-    }
-    mbar_init(smem_u32(&sm.p_full), 128);
-    mbar_init(smem_u32(&sm.pv_done), 1);
-    mbar_init(smem_u32(&sm.o_empty), 128);
-    mbar_init(smem_u32(&sm.drain), 1);
-    sm.abort_flag = 0;
-    fence_barrier_init();
-  }
-  if (warp == 1) {
-    tmem_alloc(smem_u32(&sm.tmem_base), kTmemCols);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = sm.tmem_base;
-
-  if (warp == 0) {
-    // ============================================================ TMA producer
-    if (lane == 0) {
-      tma_prefetch_desc(&tmQ);
-      tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmV);
-      bool ok = true;
-      bool issued[STAGES] = {false, false};
-      uint32_t last_ph[STAGES] = {0, 0};
-      const uint32_t qb = smem_u32(&sm.q_full);
-      mbar_arrive_expect_tx(qb, kTileBytes);
-      for (int s = 0; s < SLABS; ++s) tma_load_3d(smem_u32(sm.q + s * BM * 128), &tmQ, qb, 64 * s, hq, qt * BM);
-      for (int j = 0; j < nkv; ++j) {
-        const int st = j % STAGES;
-        const uint32_t ph = (j / STAGES) & 1;
-        if (!(ok = mbar_wait(smem_u32(&sm.k_empty[st]), ph ^ 1, abort_flag, lim, 302))) break;
-        mbar_arrive_expect_tx(smem_u32(&sm.k_full[st]), kTileBytes);
-        for (int s = 0; s < SLABS; ++s)
-          tma_load_3d(smem_u32(sm.k[st] + s * BN * 128), &tmK, smem_u32(&sm.k_full[st]), 64 * s, g, j * BN);
-        if (!(ok = mbar_wait(smem_u32(&sm.v_empty[st]), ph ^ 1, abort_flag, lim, 303))) break;
-        mbar_arrive_expect_tx(smem_u32(&sm.v_full[st]), kTileBytes);
-        for (int s = 0; s < SLABS; ++s)
-          tma_load_3d(smem_u32(sm.v[st] + s * BN * 128), &tmV, smem_u32(&sm.v_full[st]), 64 * s, g, j * BN);
-        issued[st] = true;
-        last_ph[st] = ph;
-      }
-      if (!ok) {
-        for (int s = 0; s < STAGES; ++s)
-          if (issued[s]) {
-            mbar_wait(smem_u32(&sm.k_full[s]), last_ph[s], abort_flag, 1 << 22, 0);
-            mbar_wait(smem_u32(&sm.v_full[s]), last_ph[s], abort_flag, 1 << 22, 0);
-          }
-      }
-    }
-  } else if (warp == 1) {
-    // ============================================================ MMA issuer
-    if (lane == 0) {
-      bool ok = mbar_wait(smem_u32(&sm.q_full), 0, abort_flag, lim, 310);
-      const uint32_t q_base = smem_u32(sm.q), p_base = smem_u32(sm.p);
-      uint32_t pv_cnt = 0;
-      auto do_pv = [&](int jj) -> bool {
-        const int st = jj % STAGES;
-        if (!mbar_wait(smem_u32(&sm.p_full), pv_cnt & 1, abort_flag, lim, 311)) return false;
-        if (!mbar_wait(smem_u32(&sm.v_full[st]), (jj / STAGES) & 1, abort_flag, lim, 312)) return false;
-        tc_fence_after();
-        const uint32_t v_base = smem_u32(sm.v[st]);
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk)
-          mma_bf16_ss(tmem + kColO, desc_sw128(p_base + (kk >> 2) * (BM * 128) + (kk & 3) * 32, 16, 1024),
-                      desc_sw128(v_base + kk * 16 * 128, BN * 128, 1024), kIdescO, (kk > 0 || jj > 0) ? 1u : 0u);
-        mma_commit(smem_u32(&sm.pv_done));
-        mma_commit(smem_u32(&sm.v_empty[st]));
-        ++pv_cnt;
-        return true;
-      };
-      for (int j = 0; j < nkv && ok; ++j) {
-        const int st = j % STAGES, sb = j & 1;
-        if (!(ok = mbar_wait(smem_u32(&sm.k_full[st]), (j / STAGES) & 1, abort_flag, lim, 314))) break;
-        if (!(ok = mbar_wait(smem_u32(&sm.s_empty[sb]), ((j >> 1) & 1) ^ 1, abort_flag, lim, 315))) break;
-        tc_fence_after();
-        const uint32_t k_base = smem_u32(sm.k[st]);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
-          mma_bf16_ss(tmem + kColS0 + sb * BN, desc_sw128(q_base + off, 16, 1024),
-                      desc_sw128(k_base + (kk >> 2) * (BN * 128) + (kk & 3) * 32, 16, 1024), kIdescS,
-                      kk > 0 ? 1u : 0u);
-        }
-        mma_commit(smem_u32(&sm.s_full[sb]));
-        mma_commit(smem_u32(&sm.k_empty[st]));
-        if (j > 0 && !(ok = do_pv(j - 1))) break;
-      }
-      if (ok) ok = do_pv(nkv - 1);
-      mma_commit(smem_u32(&sm.drain));
-      mbar_wait(smem_u32(&sm.drain), 0, abort_flag, ok ? lim : (1 << 22), 316);
-    }
-  } else if (warp >= 2) {
-    // ============================================================ softmax + epilogue
-    const int quarter = warp & 3;
-    const int row = quarter * 32 + lane;
-    const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    const uint32_t p_base = smem_u32(sm.p);
-    const long long qpos = p.q_pos0 + static_cast<long long>(qt) * BM + row;
-    float m = -CUDART_INF_F, l = 0.f;
-    bool ok = true;
-    for (int j = 0; j < nkv; ++j) {
-      const int sb = j & 1;
-      const int kv_valid = min(BN, p.Tk - j * BN);
-      const long long kpos0 = p.k_pos0 + static_cast<long long>(j) * BN;
-      int col_lim = kv_valid;
-      bool masked = kv_valid < BN;
-      if (p.causal) {
-        const long long vis = qpos - kpos0 + 1;   // keys of this tile visible to the row
-        col_lim = vis < 0 ? 0 : (vis > kv_valid ? kv_valid : static_cast<int>(vis));
-        masked = masked || kpos0 + kv_valid - 1 > p.q_pos0 + static_cast<long long>(qt) * BM;
-      }
-      if (!(ok = mbar_wait(smem_u32(&sm.s_full[sb]), (j >> 1) & 1, abort_flag, lim, 320))) break;
-      tc_fence_after();
-      uint32_t pk[BN / 2];
-      const float alpha = softmax_row(t_lane + kColS0 + sb * BN, j, masked, col_lim, p.scale_log2, m, l, pk);
-      tc_fence_before();
-      mbar_arrive(smem_u32(&sm.s_empty[sb]));
-      if (j > 0) {
-        // P_{j-1} V_{j-1} must be complete: P buffer reuse and O rescale
-        if (!(ok = mbar_wait(smem_u32(&sm.pv_done), (j - 1) & 1, abort_flag, lim, 321))) break;
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll
-          for (int c4 = 0; c4 < D / 32; ++c4) {
-            uint32_t orr[32];
-            tmem_ld32(t_lane + kColO + 32 * c4, orr);
-            tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
-            tmem_st32(t_lane + kColO + 32 * c4, orr);
-          }
-          tmem_wait_st();
-        }
-      }
-#pragma unroll
-      for (int ch = 0; ch < BN / 8; ++ch) {
-        const int slab = ch >> 3, c16 = ch & 7;
-        const uint32_t addr = p_base + slab * (BM * 128) + row * 128 + ((c16 ^ (row & 7)) << 4);
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[4 * ch]), "r"(pk[4 * ch + 1]),
-                     "r"(pk[4 * ch + 2]), "r"(pk[4 * ch + 3])
-                     : "memory");
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(smem_u32(&sm.p_full));
-    }
-    if (ok && mbar_wait(smem_u32(&sm.pv_done), (nkv - 1) & 1, abort_flag, lim, 322)) {
-      tc_fence_after();
-      const bool live = l > 0.f;
-      const float inv_l = live ? 1.f / l : 0.f;
-      const bool row_ok = row < q_valid;
-      float* orow = p.o + (static_cast<int64_t>(qt * BM + row) * p.Hq + hq) * D;
-#pragma unroll
-      for (int c4 = 0; c4 < D / 32; ++c4) {
-        uint32_t orr[32];
-        tmem_ld32(t_lane + kColO + 32 * c4, orr);
-        tmem_wait_ld();
-        if (row_ok) {
-#pragma unroll
-          for (int i = 0; i < 32; i += 4)
-            *reinterpret_cast<float4*>(orow + 32 * c4 + i) =
-                make_float4(__uint_as_float(orr[i]) * inv_l, __uint_as_float(orr[i + 1]) * inv_l,
-                            __uint_as_float(orr[i + 2]) * inv_l, __uint_as_float(orr[i + 3]) * inv_l);
-        }
-      }
-      if (row_ok)
-        p.lse[static_cast<int64_t>(qt * BM + row) * p.Hq + hq] = live ? (m + log2f(l)) * kLn2 : -CUDART_INF_F;
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
-}
-
 // Per-rank tile classification with the kernels' own iterator (for tests):
 // visited tiles that need no mask, visited tiles with a causal mask, skipped.
 __global__ void schedule_counts_kernel(Sched s, unsigned long long* counts) {
@@ -1130,40 +713,6 @@ __global__ void schedule_counts_kernel(Sched s, unsigned long long* counts) {
     atomicAdd(&counts[r * 3 + 1], diag);
     atomicAdd(&counts[r * 3 + 2], static_cast<unsigned long long>(2 * s.N * s.ntk) - seen);
   }
-}
-
-// ------------------------------------------------------------------ host side
-using EncodeTiledFn = decltype(&cuTensorMapEncodeTiled);
-
-EncodeTiledFn get_encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(ptr);
-  }
-  return fn;
-}
-
-// Token-major [rows, H, D] bf16 tensor; box = 64 columns x 1 head x 128 rows,
-// 128-byte swizzle (the layout the MMA descriptors expect).
-ra_status make_map(CUtensorMap* map, const void* base, int D, int H, int64_t rows, uint32_t box_rows = 128) {
-  EncodeTiledFn enc = get_encode_fn();
-  if (!enc) return ra::fail(RA_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(H) * D * 2};
-  cuuint32_t box[3] = {64, 1, box_rows};
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return ra::fail(RA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
-  return RA_OK;
 }
 
 template <int D>
@@ -1199,16 +748,7 @@ ra_status ring_attn_fwd_f32(const void* q, const void* k, const void* v, void* o
                             int Hkv, int S, int d, int causal, int N, float scale, int layout,
                             cudaStream_t stream);
 
-// Bound of every device-side wait, in SM clock cycles: ~0.5 s by default,
-// overridable with the environment variable RA_WAIT_LIMIT_CYCLES.
-static long long wait_limit() {
-  static long long lim = [] {
-    const char* e = getenv("RA_WAIT_LIMIT_CYCLES");
-    long long v = e ? atoll(e) : 0;
-    return v > 0 ? v : (1ll << 30);
-  }();
-  return lim;
-}
+
 }  // namespace ra
 
 extern "C" ra_status ra_ring_attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse,
@@ -1276,91 +816,3 @@ extern "C" ra_status ra_ring_schedule_counts(int32_t S, int32_t n_ranks, int32_t
   return ra_ring_schedule_counts_ex(S, n_ranks, causal, 128, counts, stream);
 }
 
-
-// ------------------------------------------------------------------ block partials and segmented prefill
-namespace {
-template <int D>
-ra_status launch_block(const void* q, const void* k, const void* v, const BlockParams& bp, cudaStream_t stream) {
-  CUtensorMap mq, mk, mv;
-  ra_status st;
-  if ((st = make_map(&mq, q, D, bp.Hq, bp.Tq)) != RA_OK) return st;
-  if ((st = make_map(&mk, k, D, bp.Hkv, bp.Tk)) != RA_OK) return st;
-  if ((st = make_map(&mv, v, D, bp.Hkv, bp.Tk)) != RA_OK) return st;
-  const size_t smem = sizeof(Smem<D>) + 1024;
-  RA_CUDA_TRY(cudaFuncSetAttribute(block_attn_bf16_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   static_cast<int>(smem)));
-  const int64_t grid = ra::ceil_div(bp.Tq, BM) * bp.Hq;
-  block_attn_bf16_kernel<D><<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(mq, mk, mv, bp);
-  RA_LAUNCH_CHECK("block_attn_bf16_kernel");
-  return RA_OK;
-}
-
-ra_status check_block_args(const void* q, const void* k, const void* v, int32_t Tq, int32_t Tk, int32_t Hq,
-                           int32_t Hkv, int32_t d, int64_t q_pos0, int64_t k_pos0) {
-  RA_REQUIRE(Tq >= 1 && Tk >= 1 && Hq >= 1 && Hkv >= 1, "Tq, Tk, Hq, Hkv must be >= 1");
-  RA_REQUIRE(Hq % Hkv == 0, "Hq (%d) must be a multiple of Hkv (%d)", Hq, Hkv);
-  RA_REQUIRE(q_pos0 >= 0 && k_pos0 >= 0, "positions must be >= 0");
-  if (d != 64 && d != 128) return ra::fail(RA_ERR_UNSUPPORTED, "head dim %d not supported (64 or 128)", d);
-  RA_REQUIRE(q && k && v, "NULL pointer");
-  RA_REQUIRE(ra::aligned16(q) && ra::aligned16(k) && ra::aligned16(v), "q, k, v must be 16-byte aligned");
-  RA_REQUIRE(static_cast<int64_t>(ra::ceil_div(Tq, BM)) * Hq < (int64_t(1) << 31), "grid too large");
-  return RA_OK;
-}
-}  // namespace
-
-extern "C" ra_status ra_attn_block_fwd(const void* q, const void* k, const void* v, int32_t Tq, int32_t Tk,
-                                       int32_t Hq, int32_t Hkv, int32_t d, int64_t q_pos0, int64_t k_pos0,
-                                       int32_t causal, float scale, float* o_part, float* lse_part,
-                                       ra_stream stream) {
-  ra::clear_error();
-  ra_status st = check_block_args(q, k, v, Tq, Tk, Hq, Hkv, d, q_pos0, k_pos0);
-  if (st != RA_OK) return st;
-  RA_REQUIRE(o_part && lse_part && ra::aligned16(o_part) && reinterpret_cast<uintptr_t>(lse_part) % 4 == 0,
-             "o_part must be 16-byte aligned, lse_part 4-byte aligned");
-  BlockParams bp;
-  bp.Tq = Tq; bp.Tk = Tk; bp.Hq = Hq; bp.Hkv = Hkv; bp.group = Hq / Hkv; bp.causal = causal ? 1 : 0;
-  bp.q_pos0 = q_pos0; bp.k_pos0 = k_pos0;
-  bp.scale_log2 = (scale > 0.f ? scale : 1.f / sqrtf(static_cast<float>(d))) * 1.4426950408889634f;
-  bp.o = o_part; bp.lse = lse_part; bp.wait_limit = ra::wait_limit();
-  return d == 128 ? launch_block<128>(q, k, v, bp, stream) : launch_block<64>(q, k, v, bp, stream);
-}
-
-extern "C" ra_status ra_segmented_prefill_workspace_size(int32_t Tq, int32_t Tk, int32_t Hq, int32_t d,
-                                                         int32_t seg_tokens, size_t* bytes) {
-  ra::clear_error();
-  RA_REQUIRE(bytes != nullptr, "bytes is NULL");
-  RA_REQUIRE(Tq >= 1 && Tk >= 1 && Hq >= 1 && d >= 1 && seg_tokens >= 1, "sizes must be >= 1");
-  const int64_t P = ra::ceil_div(Tk, seg_tokens);
-  const int64_t o_bytes = P * Tq * Hq * d * 4;
-  *bytes = static_cast<size_t>(ra::ceil_div(o_bytes, 256) * 256 + P * Tq * Hq * 4);
-  return RA_OK;
-}
-
-extern "C" ra_status ra_segmented_prefill_fwd(const void* q, const void* k, const void* v, int32_t Tq, int32_t Tk,
-                                              int32_t Hq, int32_t Hkv, int32_t d, int64_t q_pos0, int32_t causal,
-                                              float scale, int32_t seg_tokens, void* o, ra_dtype out_dt, float* lse,
-                                              void* workspace, size_t ws_bytes, ra_stream stream) {
-  ra::clear_error();
-  ra_status st = check_block_args(q, k, v, Tq, Tk, Hq, Hkv, d, q_pos0, 0);
-  if (st != RA_OK) return st;
-  RA_REQUIRE(seg_tokens >= 1, "seg_tokens must be >= 1");
-  RA_REQUIRE(out_dt == RA_F32 || out_dt == RA_BF16, "unknown out dtype");
-  RA_REQUIRE(o && workspace && ra::aligned16(o) && ra::aligned16(workspace), "o/workspace must be 16-byte aligned");
-  size_t need = 0;
-  if ((st = ra_segmented_prefill_workspace_size(Tq, Tk, Hq, d, seg_tokens, &need)) != RA_OK) return st;
-  RA_REQUIRE(ws_bytes >= need, "workspace too small (%zu < %zu bytes)", ws_bytes, need);
-  const int64_t P = ra::ceil_div(Tk, seg_tokens);
-  float* o_parts = static_cast<float*>(workspace);
-  float* lse_parts = reinterpret_cast<float*>(static_cast<char*>(workspace) +
-                                              ra::ceil_div(P * Tq * Hq * d * 4, 256) * 256);
-  const size_t kv_row = static_cast<size_t>(Hkv) * d * 2;
-  for (int64_t sgi = 0; sgi < P; ++sgi) {
-    const int64_t k0 = sgi * seg_tokens;
-    const int32_t tk = static_cast<int32_t>(std::min<int64_t>(seg_tokens, Tk - k0));
-    st = ra_attn_block_fwd(q, static_cast<const char*>(k) + k0 * kv_row, static_cast<const char*>(v) + k0 * kv_row,
-                           Tq, tk, Hq, Hkv, d, q_pos0, k0, causal, scale, o_parts + sgi * Tq * Hq * d,
-                           lse_parts + sgi * Tq * Hq, stream);
-    if (st != RA_OK) return st;
-  }
-  return ra_lse_merge(o_parts, lse_parts, static_cast<int32_t>(P), Tq, Hq, d, o, out_dt, lse, stream);
-}

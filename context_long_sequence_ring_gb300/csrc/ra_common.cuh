@@ -27,6 +27,7 @@ int fetch_error_cache(int* where);
 int fetch_error_decode(int* where);
 int fetch_error_attn_f32(int* where);
 int fetch_error_attn_bf16(int* where);
+int fetch_error_attn_block(int* where);
 
 }  // namespace ra
 
