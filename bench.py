@@ -330,6 +330,7 @@ def run_ours(args, rank, world, dev):
         "clocks": clk.summary(),
     }
     line["next_segmented_prefill"] = measure_segmented(ra, dev)
+    line["next_kv_reorg"] = measure_kv_reorg(ra, wl)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_rows)
     return line
@@ -388,6 +389,37 @@ def measure_segmented(ra, dev, reps=5):
     flops = 4.0 * S["Hq"] * S["d"] * pairs
     return {"config": S, "ms": round(ms, 3), "tflops": round(flops / (ms * 1e-3) / 1e12, 1),
             "frac_of_bf16_sustained": round(flops / (ms * 1e-3) / 1e12 / _peaks()["bf16_sus"], 4)}
+
+
+def measure_kv_reorg(ra, wl, n_req=8, reps=5):
+    """Reorg of the sharded cache back to contiguous per-request K/V (the next scope row after the
+    segmented prefill): every context token of the first n_req decode requests, timed alone."""
+    D = DECODE
+    ctx = wl.ctx[:n_req].cpu()
+    qsl = torch.zeros(n_req + 1, dtype=torch.int32)
+    qsl[1:] = torch.cumsum(ctx, 0)
+    pos = torch.cat([torch.arange(int(L), dtype=torch.int32) for L in ctx]).to(wl.dev)
+    qsl = qsl.to(wl.dev)
+    bt = wl.bt[:n_req].contiguous()
+    T = int(pos.numel())
+    k_out = torch.empty((T, D["Hkv"], D["d"]), dtype=torch.bfloat16, device=wl.dev)
+    v_out = torch.empty_like(k_out)
+    for _ in range(2):
+        ra.cp_kv_gather(wl.kc, wl.vc, bt, qsl, pos, D["I"], D["pcp"], D["dcp"], k_out, v_out)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        ra.cp_kv_gather(wl.kc, wl.vc, bt, qsl, pos, D["I"], D["pcp"], D["dcp"], k_out, v_out)
+    e1.record()
+    torch.cuda.synchronize()
+    if ra.device_status() != 0:
+        raise RuntimeError("device status after the KV reorg: %s" % ra.last_error())
+    ms = e0.elapsed_time(e1) / reps
+    nbytes = 2 * 2 * T * D["Hkv"] * D["d"] * 2          # K and V, read once and written once
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"requests": n_req, "tokens": T, "ms": round(ms, 3), "gbs": round(gbs, 1),
+            "frac_of_hbm": round(gbs / _peaks()["hbm"], 4)}
 
 
 # ---------------------------------------------------------------------------- oracle arm

@@ -79,7 +79,74 @@ __global__ void kv_scatter_kernel(const uint4* __restrict__ k, const uint4* __re
   }
 }
 
+// One warp per output row: locate token positions[t] of its request in the
+// sharded cache with the block-table formula and copy its Hkv*d row of K and
+// of V (the reorg that makes each request's KV contiguous again).
+__global__ void kv_gather_kernel(const uint4* __restrict__ kc, const uint4* __restrict__ vc,
+                                 const int32_t* __restrict__ block_table, int32_t max_vb,
+                                 const int32_t* __restrict__ qsl, int32_t R, const int32_t* __restrict__ positions,
+                                 int64_t T, int32_t Hkv, int32_t d_words, int32_t block_size, int32_t interleave,
+                                 int32_t W, int64_t num_blocks, uint4* __restrict__ k_out, uint4* __restrict__ v_out) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  const int64_t row_words = static_cast<int64_t>(Hkv) * d_words;
+  for (int64_t t = warp; t < T; t += nwarps) {
+    const int q = request_of(qsl, R, t);
+    const int64_t x = positions[t];
+    const int64_t V = static_cast<int64_t>(block_size) * W;
+    const int64_t vb = x / V;
+    const int64_t o = x - vb * V;
+    const int64_t lbi = o / interleave;
+    const int64_t dev = lbi % W;
+    const int64_t off = (lbi / W) * interleave + (o % interleave);
+    int64_t blk = -1;
+    if (x >= 0 && vb < max_vb) blk = block_table[static_cast<int64_t>(q) * max_vb + vb];
+    uint4* kd = k_out + t * row_words;
+    uint4* vd = v_out + t * row_words;
+    if (blk < 0 || blk >= num_blocks) {
+      if (lane == 0) ra_record_error(RA_ERR_DEVICE_BOUNDS, 12);
+      for (int64_t e = lane; e < row_words; e += 32) kd[e] = vd[e] = make_uint4(0, 0, 0, 0);
+      continue;
+    }
+    for (int64_t e = lane; e < row_words; e += 32) {
+      const int64_t g = e / d_words, u = e % d_words;
+      const int64_t src = (((dev * num_blocks + blk) * Hkv + g) * block_size + off) * d_words + u;
+      kd[e] = kc[src];
+      vd[e] = vc[src];
+    }
+  }
+}
+
 }  // namespace
+
+extern "C" ra_status ra_cp_kv_gather(const void* k_cache, const void* v_cache, const int32_t* block_table,
+                                     int32_t max_vblocks, const int32_t* query_start_loc, const int32_t* positions,
+                                     int32_t R, int64_t T, int32_t Hkv, int32_t d, int32_t block_size,
+                                     int32_t interleave, int32_t pcp, int32_t dcp, int64_t num_blocks, ra_dtype dt,
+                                     void* k_out, void* v_out, ra_stream stream) {
+  ra::clear_error();
+  RA_REQUIRE(block_size >= 1 && interleave >= 1 && pcp >= 1 && dcp >= 1,
+             "block_size, interleave, pcp and dcp must be >= 1");
+  RA_REQUIRE(block_size % interleave == 0,
+             "block_size %% cp_kv_cache_interleave_size must be 0 (block_size=%d, interleave=%d)",
+             block_size, interleave);
+  RA_REQUIRE(R >= 1 && T >= 0 && max_vblocks >= 1 && Hkv >= 1 && d >= 1 && num_blocks >= 1, "sizes must be positive");
+  RA_REQUIRE(dt == RA_BF16 || dt == RA_F32, "unknown dtype");
+  const int64_t row_bytes = static_cast<int64_t>(d) * (dt == RA_BF16 ? 2 : 4);
+  if (row_bytes % 16 != 0) return ra::fail(RA_ERR_UNSUPPORTED, "d*elem_size must be a multiple of 16");
+  if (T == 0) return RA_OK;
+  RA_REQUIRE(k_cache && v_cache && block_table && query_start_loc && positions && k_out && v_out, "NULL pointer");
+  RA_REQUIRE(ra::aligned16(k_cache) && ra::aligned16(v_cache) && ra::aligned16(k_out) && ra::aligned16(v_out),
+             "cache and output pointers must be 16-byte aligned");
+  const int64_t blocks = std::min<int64_t>(ra::ceil_div(T * 32, 256), 152 * 32);
+  kv_gather_kernel<<<blocks, 256, 0, stream>>>(
+      static_cast<const uint4*>(k_cache), static_cast<const uint4*>(v_cache), block_table, max_vblocks,
+      query_start_loc, R, positions, T, Hkv, static_cast<int32_t>(row_bytes / 16), block_size, interleave, pcp * dcp,
+      num_blocks, static_cast<uint4*>(k_out), static_cast<uint4*>(v_out));
+  RA_LAUNCH_CHECK("kv_gather_kernel");
+  return RA_OK;
+}
 
 extern "C" ra_status ra_cp_slot_mapping(const int32_t* query_start_loc, const int32_t* positions,
                                         const int32_t* block_table, int32_t max_vblocks, int32_t R,

@@ -41,6 +41,8 @@ SIGNATURES = {
                                  _c.c_int, _vp, _vp, _sz, _vp],
     "ra_cp_slot_mapping": [_vp, _vp, _vp, _i32, _i32, _i64, _i32, _i32, _i32, _i32, _vp, _vp],
     "ra_cp_kv_scatter": [_vp, _vp, _vp, _vp, _vp, _i64, _i32, _i32, _i32, _i32, _i64, _c.c_int, _vp],
+    "ra_cp_kv_gather": [_vp, _vp, _vp, _i32, _vp, _vp, _i32, _i64, _i32, _i32, _i32, _i32, _i32, _i32, _i64,
+                        _c.c_int, _vp, _vp, _vp],
     "ra_cp_decode_workspace_size": [_i32, _i32, _i32, _i32, _i32, _i32, _i32, _c.POINTER(_sz)],
     "ra_cp_decode": [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i64, _f32,
                      _i32, _vp, _c.c_int, _vp, _vp, _sz, _vp],
@@ -251,6 +253,22 @@ def cp_kv_scatter(k, v, slot, k_cache, v_cache):
     W, NB, Hkv, bs, d = k_cache.shape
     _check(lib().ra_cp_kv_scatter(_ptr(k), _ptr(v), _ptr(slot), _ptr(k_cache), _ptr(v_cache), k.shape[0], W, Hkv,
                                   d, bs, NB, _dt(k), _stream()))
+
+
+def cp_kv_gather(k_cache, v_cache, block_table, query_start_loc, positions, interleave: int, pcp: int, dcp: int,
+                 k_out=None, v_out=None):
+    """Token rows out of the sharded cache: row t = token positions[t] of its request -> (k [T, Hkv, d], v)."""
+    _need_cuda(k_cache, v_cache, block_table, query_start_loc, positions, k_out, v_out)
+    W, NB, Hkv, bs, d = k_cache.shape
+    T = positions.numel()
+    if k_out is None:
+        k_out = torch.empty((T, Hkv, d), dtype=k_cache.dtype, device=k_cache.device)
+    if v_out is None:
+        v_out = torch.empty_like(k_out)
+    _check(lib().ra_cp_kv_gather(_ptr(k_cache), _ptr(v_cache), _ptr(block_table), block_table.shape[1],
+                                 _ptr(query_start_loc), _ptr(positions), query_start_loc.numel() - 1, T, Hkv, d, bs,
+                                 interleave, pcp, dcp, NB, _dt(k_cache), _ptr(k_out), _ptr(v_out), _stream()))
+    return k_out, v_out
 
 
 def cp_decode_workspace_size(R, Hq, d, max_vblocks, pcp, dcp, split_blocks) -> int:

@@ -256,6 +256,27 @@ ra_status ra_cp_kv_scatter(const void* k, const void* v, const int32_t* slot, vo
                            int32_t block_size, int64_t num_blocks, ra_dtype dt, ra_stream stream);
 
 /* ------------------------------------------------------------------------
+ * ra_cp_kv_gather -- read token rows back out of the sharded paged cache in
+ * any order: the reorg that makes each request's KV contiguous after the
+ * context all-gather (vLLM-Ascend "Context Parallel (CP)", DCP chunked
+ * prefill, MLA backend: all_gather of the context KV, then reorg_kvcache).
+ * Row t of the outputs is token positions[t] of its request (query_start_loc
+ * as in ra_cp_slot_mapping), located with the block-table formula.
+ *
+ * k_cache, v_cache device [W, num_blocks, Hkv, block_size, d] (dtype dt).
+ * k_out, v_out     device [T, Hkv, d] out.
+ * A virtual block >= max_vblocks or a block id outside [0, num_blocks) is a
+ * device bounds error (the row is zero-filled).  block_size % interleave != 0
+ * -> RA_ERR_INVALID_ARG.
+ * ---------------------------------------------------------------------- */
+ra_status ra_cp_kv_gather(const void* k_cache, const void* v_cache, const int32_t* block_table,
+                          int32_t max_vblocks, const int32_t* query_start_loc,
+                          const int32_t* positions, int32_t R, int64_t T, int32_t Hkv, int32_t d,
+                          int32_t block_size, int32_t interleave, int32_t pcp, int32_t dcp,
+                          int64_t num_blocks, ra_dtype dt, void* k_out, void* v_out,
+                          ra_stream stream);
+
+/* ------------------------------------------------------------------------
  * ra_cp_decode -- one-token decode over the sharded paged cache: split-KV
  * partials per (request, device, split) followed by ra_lse_merge.
  * Source: vLLM-Ascend "Context Parallel (CP)", DCP decode and PCP decode

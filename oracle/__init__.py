@@ -37,7 +37,7 @@ from .attention import (full_attention, attention_rows, attention_block, segment
                         ring_attention, ring_partials, lse_merge, rank_chunks,
                         causal_pairs_per_rank, causal_tiles_per_rank)
 from .partition import zigzag_partition, gather_rows
-from .kvcache import (cp_slot_mapping, cp_token_location, cp_kv_scatter,
+from .kvcache import (cp_slot_mapping, cp_token_location, cp_kv_scatter, cp_kv_gather,
                       cp_decode, cp_decode_partials, decode_reference)
 
 __all__ = [
@@ -45,5 +45,5 @@ __all__ = [
     "ring_attention", "ring_partials",
     "lse_merge", "rank_chunks", "causal_pairs_per_rank", "causal_tiles_per_rank",
     "zigzag_partition", "gather_rows", "cp_slot_mapping", "cp_token_location",
-    "cp_kv_scatter", "cp_decode", "cp_decode_partials", "decode_reference",
+    "cp_kv_scatter", "cp_kv_gather", "cp_decode", "cp_decode_partials", "decode_reference",
 ]

@@ -92,6 +92,31 @@ def cp_kv_scatter(k, v, slot, k_cache, v_cache, block_size: int):
         v_cache[w, s // block_size, :, s % block_size, :] = v[ts]
 
 
+def cp_kv_gather(k_cache, v_cache, block_table, query_start_loc, positions, block_size: int,
+                 interleave: int, pcp: int, dcp: int):
+    """Rows of the sharded cache back in token order (the reorg that makes
+    each request's KV contiguous after the context all-gather; vLLM-Ascend
+    "Context Parallel (CP)", DCP chunked prefill, MLA: all_gather of the
+    context KV, then reorg_kvcache).  Output row t holds the K/V of token
+    positions[t] of its request, read from the device and offset the
+    block-table formula assigns to it.  Returns (k [T, Hkv, d], v [T, Hkv, d]).
+    """
+    _check(block_size, interleave, pcp, dcp)
+    qsl = np.asarray(query_start_loc, dtype=np.int64)
+    pos = np.asarray(positions, dtype=np.int64)
+    bt = np.asarray(block_table, dtype=np.int64)
+    T = len(pos)
+    req = np.searchsorted(qsl, np.arange(T), side="right") - 1
+    out_k = np.zeros((T,) + k_cache.shape[2:3] + k_cache.shape[4:], dtype=k_cache.dtype)
+    out_v = np.zeros_like(out_k)
+    for t in range(T):
+        vb, dev, off = cp_token_location(int(pos[t]), block_size, interleave, pcp, dcp)
+        blk = bt[req[t], vb]
+        out_k[t] = k_cache[dev, blk, :, off, :]
+        out_v[t] = v_cache[dev, blk, :, off, :]
+    return out_k, out_v
+
+
 def _device_tokens(w, vb, block_size, interleave, W):
     """Token index x (within the request) held in local slot j of device w, virtual block vb."""
     j = np.arange(block_size)
@@ -158,5 +183,5 @@ def decode_reference(q_row, k_tokens, v_tokens, scale=None):
     return o[0], lse[0]
 
 
-__all__ = ["cp_token_location", "cp_slot_mapping", "cp_kv_scatter", "cp_decode_partials",
-           "cp_decode", "decode_reference"]
+__all__ = ["cp_token_location", "cp_slot_mapping", "cp_kv_scatter", "cp_kv_gather",
+           "cp_decode_partials", "cp_decode", "decode_reference"]

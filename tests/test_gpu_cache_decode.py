@@ -224,3 +224,33 @@ def test_decode_full_size_sampled_requests(ra):
         vr = I.synth_rows(seed, I.TID_V, rows, Hkv * d, torch.bfloat16).reshape(-1, Hkv, d)
         O, L = oracle.decode_reference(qd[r], kr, vr)
         assert_parity(o[r], O, lse[r], L, torch.bfloat16, "full-size decode request %d" % r)
+
+
+# --------------------------------------------------------------------- cache reorg (gather)
+
+def test_kv_gather_round_trip_and_oracle(ra):
+    """Scatter into the sharded cache, gather back in token order: bit-exact, and equal to the
+    oracle's gather from the same cache; a reversed order works too."""
+    wl, kt, vt, qd, qsl, slot, kc, vc, o, lse = _decode_case(ra, 9, 3, 10, 900, 32, 8, 2, 2, 4, 2, 128, 2)
+    ctx = wl["ctx_lens"]
+    pos = torch.cat([torch.arange(int(L), dtype=torch.int32) for L in ctx])
+    k2, v2 = ra.cp_kv_gather(kc, vc, wl["block_table"].to(DEV), qsl.to(DEV), pos.to(DEV), 8, 2, 2)
+    check_status(ra)
+    assert torch.equal(k2.cpu(), kt) and torch.equal(v2.cpu(), vt)
+    n = int(ctx[1])
+    q2 = torch.tensor([0, 0, n, n], dtype=torch.int32)
+    p2 = torch.arange(n - 1, -1, -1, dtype=torch.int32)
+    k3, v3 = ra.cp_kv_gather(kc, vc, wl["block_table"].to(DEV), q2.to(DEV), p2.to(DEV), 8, 2, 2)
+    kr, vr = oracle.cp_kv_gather(kc.float().cpu().numpy(), vc.float().cpu().numpy(), wl["block_table"].numpy(),
+                                 q2.numpy(), p2.numpy(), 32, 8, 2, 2)
+    assert np.array_equal(k3.float().cpu().numpy(), kr) and np.array_equal(v3.float().cpu().numpy(), vr)
+
+
+def test_kv_gather_bad_block_is_reported(ra):
+    kc = torch.zeros((2, 3, 1, 16, 64), dtype=torch.bfloat16, device=DEV)
+    bt = torch.tensor([[0, 7]], dtype=torch.int32, device=DEV)      # block 7 does not exist
+    qsl = torch.tensor([0, 2], dtype=torch.int32, device=DEV)
+    pos = torch.tensor([0, 40], dtype=torch.int32, device=DEV)      # token 40 is in virtual block 1
+    k, v = ra.cp_kv_gather(kc, kc, bt, qsl, pos, 8, 2, 1)
+    assert ra.device_status() == ra.RA_ERR_DEVICE_BOUNDS
+    assert torch.equal(k[1].cpu(), torch.zeros_like(k[1].cpu()))

@@ -147,3 +147,25 @@ def test_planted_slot_formula_mistake_is_caught(monkeypatch):
     s0, s1 = c["qsl"][r], c["qsl"][r + 1]
     Or, _ = oracle.decode_reference(c["q"][r], c["k"][s0:s1], c["v"][s0:s1])
     assert not np.allclose(O[r], Or, atol=1e-6)
+
+
+def test_kv_gather_inverts_the_scatter():
+    """Scatter (driven by the per-device slot arrays) then gather (driven by the location
+    formula directly) returns every token's K/V row: the two directions of the block-table
+    formula agree."""
+    c = _tiny_decode_case(seed=3)
+    k, v = oracle.cp_kv_gather(c["kc"], c["vc"], c["bt"], c["qsl"],
+                               np.concatenate([np.arange(L) for L in c["ctx"]]), c["bs"], c["I"], c["pcp"], c["dcp"])
+    np.testing.assert_array_equal(k, c["k"])
+    np.testing.assert_array_equal(v, c["v"])
+
+
+def test_kv_gather_reorders_requests():
+    """Rows come out in whatever order the positions ask for: request 2's tokens backwards."""
+    c = _tiny_decode_case(seed=4)
+    n2 = int(c["ctx"][2])
+    k2, v2 = oracle.cp_kv_gather(c["kc"], c["vc"], c["bt"], [0, 0, 0, n2], np.arange(n2)[::-1], c["bs"], c["I"],
+                                 c["pcp"], c["dcp"])
+    s2 = int(c["qsl"][2])
+    np.testing.assert_array_equal(k2, c["k"][s2:s2 + n2][::-1])
+    np.testing.assert_array_equal(v2, c["v"][s2:s2 + n2][::-1])
