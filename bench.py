@@ -37,7 +37,7 @@ METRIC = "ring-attn fwd TFLOP/s (causal-adj) & % bf16 peak; decode+merge GB/s % 
 PREFILL = dict(B=1, Hq=32, Hkv=8, S=131072, d=128, N=16, seed=5)
 DECODE = dict(R=64, lo=4096, hi=131072, Hq=32, Hkv=8, d=128, bs=128, I=16, pcp=2, dcp=4, seed=4, split=8)
 # sources whose contents the recorded DRAM traffic of each kernel was measured on
-KERNEL_SOURCES = {"ring_attn_bf16": ["ra_attn_bf16.cu", "ra_attn_tc.cuh", "ra_sm100.cuh"],
+KERNEL_SOURCES = {"ring_attn_bf16": ["ra_attn_bf16.cu", "ra_attn_pair.cuh", "ra_attn_tc.cuh", "ra_sm100.cuh"],
                   "cp_decode": ["ra_decode.cu"]}
 
 
@@ -318,7 +318,8 @@ def run_ours(args, rank, world, dev):
         },
         "roofline": {"bound": "tensor", "achieved": round(attn_tflops, 1), "peak": pk["bf16_sus"], "unit": "TFLOP/s",
                      "frac": round(attn_tflops / pk["bf16_sus"], 4), "traffic": _traffic("ring_attn_bf16"),
-                     "kernel": "ring_attn_bf16_kernel", "peak_kind": "bf16 dense sustained (%s)" % pk["src"],
+                     "kernel": "attn_pair_kernel<RingPolicy> (ring order, two GQA heads per CTA)",
+                     "peak_kind": "bf16 dense sustained (%s)" % pk["src"],
                      "algorithmic": "%.4g FLOP per launch" % flops},
         "roofline_decode": {"bound": "hbm", "achieved": round(dec_gbs, 1), "peak": pk["hbm"], "unit": "GB/s",
                             "frac": round(dec_gbs / pk["hbm"], 4), "traffic": _traffic("cp_decode"),

@@ -36,7 +36,7 @@
 // S_{j+1}.  O is rescaled in tensor memory only when a row's running max grows
 // by more than 2^8 (the stale max is exact as long as l and O use the same
 // reference and P stays in range).
-#include "ra_attn_tc.cuh"
+#include "ra_attn_pair.cuh"
 
 RA_DEFINE_ERROR_FETCH(fetch_error_attn_bf16)
 
@@ -95,7 +95,7 @@ __device__ __forceinline__ void tile_mask(const Sched& s, int qc, int qi, int kc
 }
 
 struct Params {
-  int B, Hq, Hkv, S, N, c, nt, causal, layout, group;
+  int B, Hq, Hkv, S, N, c, nt, causal, layout, group, d;
   float scale_log2;
   __nv_bfloat16* o;
   float* lse;
@@ -387,22 +387,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-// ===========================================================================
-// Two-head variant for GQA (Hq/Hkv even): a CTA runs two query heads that read
-// the same K/V head, so every K/V tile TMA brings in feeds two score tiles.
-// Roles (384 threads): warp 0 TMA, warp 1 TMEM allocation + MMA issue, warps
-// 4..7 softmax of head 0, warps 8..11 softmax of head 1 (warps 2, 3 idle).
-// Tensor memory: S_h = cols [128h, 128h+128), O_h = cols [256+128h, ...).
-// P_h (bf16, two per column) overwrites the first 64 columns of S_h and is
-// the A operand of O_h += P_h V straight from tensor memory, so P never
-// touches shared memory.  One thread issues every MMA, in the order
-//   PV0_j, S0_{j+1}, PV1_j, S1_{j+1}
-// which staggers the two heads: each softmax warpgroup works while the tensor
-// core serves the other head (measured faster than one issuer per head).
-// tcgen05 operations of one thread execute in issue order, so S_h(j+1) may
-// overwrite the columns PV_h(j) reads.  A softmax warpgroup only waits for
-// the previous P.V when it must rescale O (lazy rescale, threshold 2^8).
-// ===========================================================================
 struct Item2 {
   int b, hq0, g, r, j;
 };
@@ -418,278 +402,59 @@ __device__ __forceinline__ Item2 decode_item2(const Params& p, int idx) {
   return it;
 }
 
-template <int D>
-struct __align__(1024) Smem2 {
-  uint8_t q[2][BM * D * 2];
-  uint8_t k[STAGES][BN * D * 2];
-  uint8_t v[STAGES][BN * D * 2];
-  uint64_t q_full, q_empty, k_full[STAGES], k_empty[STAGES], v_full[STAGES], v_empty[STAGES];
-  uint64_t s_full[2], p_full[2], pv_done[2], o_empty[2], drain;
-  uint32_t tmem_base;
-  int abort_flag;
+
+// Ring schedule: a mirrored pair of query tiles of one virtual rank, K/V tiles
+// in ring order, causal mask by original position, bf16 output.
+struct RingPolicy {
+  using Args = Params;
+  struct KvPos {
+    KvIter it;
+    int kc, kt;
+    int32_t row;
+  };
+  const Params& p;
+  Item2 item;
+  Sched sch;
+  int qc, qi;
+  __device__ RingPolicy(const Params& a, int idx)
+      : p(a), item(decode_item2(a, idx)), sch{a.N, a.c, a.nt, a.causal, BN, a.nt}, qc(0), qi(0) {}
+  __device__ int tiles() const { return 2; }
+  __device__ int hq0() const { return item.hq0; }
+  __device__ int kvh() const { return item.g; }
+  __device__ void set_tile(int ti) {
+    const Item it1{item.b, item.hq0, item.g, item.r, item.j};
+    tile_of(p, it1, ti, qc, qi);
+  }
+  __device__ int32_t q_row() const { return static_cast<int32_t>(token_row(p, item.b, qc, qi * BM)); }
+  __device__ int q_valid() const { return min(BM, p.c - qi * BM); }
+  __device__ int n_kv() const { return n_kv_tiles(sch, qc, qi); }
+  __device__ void kv_begin(KvPos& k) const { k.it.init(sch, qc, qi); }
+  __device__ bool kv_next(KvPos& k) const {
+    if (!k.it.next(k.kc, k.kt)) return false;
+    k.row = static_cast<int32_t>(token_row(p, item.b, k.kc, k.kt * BN));
+    return true;
+  }
+  __device__ void mask(const KvPos& k, int row, int& col_lim, bool& masked) const {
+    tile_mask(sch, qc, qi, k.kc, k.kt, row, col_lim, masked);
+  }
+  __device__ void store_o(int h, int row, int col0, const uint32_t (&o)[32], float inv_l) const {
+    const int64_t trow = token_row(p, item.b, qc, qi * BM + row);
+    __nv_bfloat16* dst = p.o + (trow * p.Hq + item.hq0 + h) * (p.d) + col0;
+#pragma unroll
+    for (int i = 0; i < 32; i += 8) {
+      uint4 pk;
+      pk.x = f2_bf16x2(__uint_as_float(o[i]) * inv_l, __uint_as_float(o[i + 1]) * inv_l);
+      pk.y = f2_bf16x2(__uint_as_float(o[i + 2]) * inv_l, __uint_as_float(o[i + 3]) * inv_l);
+      pk.z = f2_bf16x2(__uint_as_float(o[i + 4]) * inv_l, __uint_as_float(o[i + 5]) * inv_l);
+      pk.w = f2_bf16x2(__uint_as_float(o[i + 6]) * inv_l, __uint_as_float(o[i + 7]) * inv_l);
+      *reinterpret_cast<uint4*>(dst + i) = pk;
+    }
+  }
+  __device__ void store_lse(int h, int row, float lse) const {
+    p.lse[token_row(p, item.b, qc, qi * BM + row) * p.Hq + item.hq0 + h] = lse;
+  }
+  __device__ void write_empty(int, int) const {}  // every ring query tile meets at least one key tile
 };
-
-constexpr int kThreads2 = 384;
-
-template <int D>
-__global__ void __launch_bounds__(kThreads2, 1)
-    ring_attn_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                               const __grid_constant__ CUtensorMap tmV, const Params p) {
-  constexpr int SLABS = D / 64;
-  constexpr uint32_t kTileBytes = BM * D * 2;
-  constexpr uint32_t kIdescS = idesc_bf16_f32(BM, BN, 0, 0);
-  constexpr uint32_t kIdescO = idesc_bf16_f32(BM, D, 0, 1);
-
-  extern __shared__ uint8_t smem_raw[];
-  Smem2<D>& sm = *reinterpret_cast<Smem2<D>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const Item2 it = decode_item2(p, blockIdx.x);
-  const Item it1{it.b, it.hq0, it.g, it.r, it.j};   // for tile_of()
-  const Sched sch{p.N, p.c, p.nt, p.causal, BN, p.nt};
-  volatile int* abort_flag = &sm.abort_flag;
-  const long long lim = p.wait_limit;
-
-  if (threadIdx.x == 0) {
-    mbar_init(smem_u32(&sm.q_full), 1);
-    mbar_init(smem_u32(&sm.q_empty), 1);
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(smem_u32(&sm.k_full[s]), 1);
-      mbar_init(smem_u32(&sm.k_empty[s]), 1);
-      mbar_init(smem_u32(&sm.v_full[s]), 1);
-      mbar_init(smem_u32(&sm.v_empty[s]), 1);
-    }
-    for (int h = 0; h < 2; ++h) {
-      mbar_init(smem_u32(&sm.s_full[h]), 1);
-      mbar_init(smem_u32(&sm.p_full[h]), 128);
-      mbar_init(smem_u32(&sm.pv_done[h]), 1);
-      mbar_init(smem_u32(&sm.o_empty[h]), 128);
-    }
-    mbar_init(smem_u32(&sm.drain), 1);
-    sm.abort_flag = 0;
-    fence_barrier_init();
-  }
-  if (warp == 1) {
-    tmem_alloc(smem_u32(&sm.tmem_base), kTmemCols);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = sm.tmem_base;
-
-  if (warp == 0) {
-    // ============================================================ TMA producer
-    if (lane == 0) {
-      tma_prefetch_desc(&tmQ);
-      tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmV);
-      uint32_t kv_cnt = 0;
-      bool issued[STAGES] = {false, false};
-      uint32_t last_ph[STAGES] = {0, 0};
-      bool ok = true;
-      for (int ti = 0; ti < 2 && ok; ++ti) {
-        int qc, qi;
-        tile_of(p, it1, ti, qc, qi);
-        if (!(ok = mbar_wait(smem_u32(&sm.q_empty), (ti & 1) ^ 1, abort_flag, lim, 101))) break;
-        const uint32_t qb = smem_u32(&sm.q_full);
-        mbar_arrive_expect_tx(qb, 2 * kTileBytes);
-        const int32_t qrow = static_cast<int32_t>(token_row(p, it.b, qc, qi * BM));
-        for (int h = 0; h < 2; ++h)
-          for (int s = 0; s < SLABS; ++s)
-            tma_load_3d(smem_u32(sm.q[h] + s * BM * 128), &tmQ, qb, 64 * s, it.hq0 + h, qrow);
-        KvIter kv;
-        kv.init(sch, qc, qi);
-        int kc, kt;
-        while (kv.next(kc, kt)) {
-          const int st = kv_cnt % STAGES;
-          const uint32_t ph = (kv_cnt / STAGES) & 1;
-          const int32_t krow = static_cast<int32_t>(token_row(p, it.b, kc, kt * BN));
-          if (!(ok = mbar_wait(smem_u32(&sm.k_empty[st]), ph ^ 1, abort_flag, lim, 102))) break;
-          mbar_arrive_expect_tx(smem_u32(&sm.k_full[st]), kTileBytes);
-          for (int s = 0; s < SLABS; ++s)
-            tma_load_3d(smem_u32(sm.k[st] + s * BN * 128), &tmK, smem_u32(&sm.k_full[st]), 64 * s, it.g, krow);
-          if (!(ok = mbar_wait(smem_u32(&sm.v_empty[st]), ph ^ 1, abort_flag, lim, 103))) break;
-          mbar_arrive_expect_tx(smem_u32(&sm.v_full[st]), kTileBytes);
-          for (int s = 0; s < SLABS; ++s)
-            tma_load_3d(smem_u32(sm.v[st] + s * BN * 128), &tmV, smem_u32(&sm.v_full[st]), 64 * s, it.g, krow);
-          issued[st] = true;
-          last_ph[st] = ph;
-          ++kv_cnt;
-        }
-      }
-      if (!ok) {
-        for (int s = 0; s < STAGES; ++s)
-          if (issued[s]) {
-            mbar_wait(smem_u32(&sm.k_full[s]), last_ph[s], abort_flag, 1 << 22, 0);
-            mbar_wait(smem_u32(&sm.v_full[s]), last_ph[s], abort_flag, 1 << 22, 0);
-          }
-      }
-    }
-  } else if (warp == 1) {
-    // ============================================================ MMA issuer
-    if (lane == 0) {
-      uint32_t kv_cnt = 0, pf_cnt[2] = {0, 0};
-      bool ok = true;
-      // descriptors of k-step 0; a k-step adds its byte offset / 16 to the start-address field
-      const uint64_t dq[2] = {desc_sw128(smem_u32(sm.q[0]), 16, 1024), desc_sw128(smem_u32(sm.q[1]), 16, 1024)};
-      const uint64_t dk[STAGES] = {desc_sw128(smem_u32(sm.k[0]), 16, 1024), desc_sw128(smem_u32(sm.k[1]), 16, 1024)};
-      const uint64_t dv[STAGES] = {desc_sw128(smem_u32(sm.v[0]), BN * 128, 1024),
-                                   desc_sw128(smem_u32(sm.v[1]), BN * 128, 1024)};
-      auto issue_s = [&](int h, int st) {
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off16 = ((kk >> 2) * (BM * 128) + (kk & 3) * 32) >> 4;
-          mma_bf16_ss(tmem + h * BN, dq[h] + off16, dk[st] + off16, kIdescS, kk > 0 ? 1u : 0u);
-        }
-        mma_commit(smem_u32(&sm.s_full[h]));
-      };
-      auto issue_pv = [&](int h, int st, bool first) {
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk)
-          mma_bf16_ts(tmem + kColO + h * D, tmem + h * BN + kk * 8, dv[st] + ((kk * 16 * 128) >> 4), kIdescO,
-                      (kk > 0 || !first) ? 1u : 0u);
-        mma_commit(smem_u32(&sm.pv_done[h]));
-      };
-      for (int ti = 0; ti < 2 && ok; ++ti) {
-        int qc, qi;
-        tile_of(p, it1, ti, qc, qi);
-        const int nkv = n_kv_tiles(sch, qc, qi);
-        if (!(ok = mbar_wait(smem_u32(&sm.q_full), ti & 1, abort_flag, lim, 110))) break;
-        // prologue: both score tiles of K/V tile 0
-        {
-          const int st = kv_cnt % STAGES;
-          if (!(ok = mbar_wait(smem_u32(&sm.k_full[st]), (kv_cnt / STAGES) & 1, abort_flag, lim, 111))) break;
-          tc_fence_after();
-          issue_s(0, st);
-          issue_s(1, st);
-          mma_commit(smem_u32(&sm.k_empty[st]));
-          if (nkv == 1) mma_commit(smem_u32(&sm.q_empty));
-        }
-        for (int j = 0; j < nkv && ok; ++j) {
-          const uint32_t c = kv_cnt + j;
-          const int st = c % STAGES;
-          const uint32_t ph = (c / STAGES) & 1;
-          const bool more = j + 1 < nkv;
-          const int st1 = (c + 1) % STAGES;
-          const uint32_t ph1 = ((c + 1) / STAGES) & 1;
-          // O_0 += P_0 V_j
-          if (!(ok = mbar_wait(smem_u32(&sm.p_full[0]), pf_cnt[0] & 1, abort_flag, lim, 112))) break;
-          ++pf_cnt[0];
-          if (!(ok = mbar_wait(smem_u32(&sm.v_full[st]), ph, abort_flag, lim, 113))) break;
-          if (j == 0 && !(ok = mbar_wait(smem_u32(&sm.o_empty[0]), (ti & 1) ^ 1, abort_flag, lim, 114))) break;
-          tc_fence_after();
-          issue_pv(0, st, j == 0);
-          // S_0 of tile j+1
-          if (more) {
-            if (!(ok = mbar_wait(smem_u32(&sm.k_full[st1]), ph1, abort_flag, lim, 115))) break;
-            tc_fence_after();
-            issue_s(0, st1);
-          }
-          // O_1 += P_1 V_j
-          if (!(ok = mbar_wait(smem_u32(&sm.p_full[1]), pf_cnt[1] & 1, abort_flag, lim, 116))) break;
-          ++pf_cnt[1];
-          if (j == 0 && !(ok = mbar_wait(smem_u32(&sm.o_empty[1]), (ti & 1) ^ 1, abort_flag, lim, 117))) break;
-          tc_fence_after();
-          issue_pv(1, st, j == 0);
-          mma_commit(smem_u32(&sm.v_empty[st]));
-          if (more) {
-            issue_s(1, st1);
-            mma_commit(smem_u32(&sm.k_empty[st1]));
-            if (j + 1 == nkv - 1) mma_commit(smem_u32(&sm.q_empty));
-          }
-        }
-        kv_cnt += nkv;
-      }
-      mma_commit(smem_u32(&sm.drain));
-      mbar_wait(smem_u32(&sm.drain), 0, abort_flag, ok ? lim : (1 << 22), 118);
-    }
-  } else if (warp >= 4) {
-    // ============================================================ softmax + epilogue (head h)
-    const int h = (warp - 4) >> 2;
-    const int quarter = warp & 3;
-    const int row = quarter * 32 + lane;
-    const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    const uint32_t colS = h * BN, colO = kColO + h * D;
-    const int hq = it.hq0 + h;
-    uint32_t s_cnt = 0, pv_base = 0;
-    bool ok = true;
-    for (int ti = 0; ti < 2 && ok; ++ti) {
-      int qc, qi;
-      tile_of(p, it1, ti, qc, qi);
-      const int q_valid = min(BM, p.c - qi * BM);
-      const int nkv = n_kv_tiles(sch, qc, qi);
-      KvIter kv;
-      kv.init(sch, qc, qi);
-      float m = -CUDART_INF_F, l = 0.f;
-      for (int j = 0; j < nkv; ++j) {
-        int kc = 0, kt = 0;
-        kv.next(kc, kt);
-        if (!(ok = mbar_wait(smem_u32(&sm.s_full[h]), s_cnt & 1, abort_flag, lim, 120 + h))) break;
-        ++s_cnt;
-        tc_fence_after();
-        int col_lim;
-        bool masked;
-        tile_mask(sch, qc, qi, kc, kt, row, col_lim, masked);
-        uint32_t pk[BN / 2];
-        const float alpha = softmax_row(t_lane + colS, j, masked, col_lim, p.scale_log2, m, l, pk);
-        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-          // O_h must hold P_{j-1} V_{j-1} before it is rescaled
-          if (!(ok = mbar_wait(smem_u32(&sm.pv_done[h]), (pv_base + j - 1) & 1, abort_flag, lim, 124 + h))) break;
-          tc_fence_after();
-#pragma unroll
-          for (int c4 = 0; c4 < D / 32; ++c4) {
-            uint32_t orr[32];
-            tmem_ld32(t_lane + colO + 32 * c4, orr);
-            tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
-            tmem_st32(t_lane + colO + 32 * c4, orr);
-          }
-        }
-        // P_h into the first 64 columns of S_h
-        tmem_st32(t_lane + colS, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
-        tmem_st32(t_lane + colS + 32, *reinterpret_cast<const uint32_t(*)[32]>(&pk[32]));
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(smem_u32(&sm.p_full[h]));
-      }
-      if (!ok) break;
-      // ---------------------------------------------------------- epilogue
-      if (!(ok = mbar_wait(smem_u32(&sm.pv_done[h]), (pv_base + nkv - 1) & 1, abort_flag, lim, 126 + h))) break;
-      pv_base += nkv;
-      tc_fence_after();
-      const float inv_l = l > 0.f ? 1.f / l : 0.f;
-      const bool row_ok = row < q_valid;
-      const int64_t trow = token_row(p, it.b, qc, qi * BM + row);
-      __nv_bfloat16* orow = p.o + (trow * p.Hq + hq) * D;
-#pragma unroll
-      for (int c4 = 0; c4 < D / 32; ++c4) {
-        uint32_t orr[32];
-        tmem_ld32(t_lane + colO + 32 * c4, orr);
-        tmem_wait_ld();
-        if (row_ok) {
-#pragma unroll
-          for (int i = 0; i < 32; i += 8) {
-            uint4 pk;
-            pk.x = f2_bf16x2(__uint_as_float(orr[i]) * inv_l, __uint_as_float(orr[i + 1]) * inv_l);
-            pk.y = f2_bf16x2(__uint_as_float(orr[i + 2]) * inv_l, __uint_as_float(orr[i + 3]) * inv_l);
-            pk.z = f2_bf16x2(__uint_as_float(orr[i + 4]) * inv_l, __uint_as_float(orr[i + 5]) * inv_l);
-            pk.w = f2_bf16x2(__uint_as_float(orr[i + 6]) * inv_l, __uint_as_float(orr[i + 7]) * inv_l);
-            *reinterpret_cast<uint4*>(orow + 32 * c4 + i) = pk;
-          }
-        }
-      }
-      tc_fence_before();
-      mbar_arrive(smem_u32(&sm.o_empty[h]));
-      if (row_ok) p.lse[trow * p.Hq + hq] = l > 0.f ? (m + log2f(l)) * kLn2 : -CUDART_INF_F;
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
-}
 
 // Per-rank tile classification with the kernels' own iterator (for tests):
 // visited tiles that need no mask, visited tiles with a causal mask, skipped.
@@ -727,10 +492,10 @@ ra_status launch_bf16(const void* q, const void* k, const void* v, const Params&
   const int64_t tiles = static_cast<int64_t>(prm.B) * prm.Hq * prm.N * prm.nt;  // mirrored tile pairs x heads
   if (variant == 2) {
     const size_t smem = sizeof(Smem2<D>) + 1024;
-    RA_CUDA_TRY(cudaFuncSetAttribute(ring_attn_bf16_pair_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    RA_CUDA_TRY(cudaFuncSetAttribute(attn_pair_kernel<D, RingPolicy>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      static_cast<int>(smem)));
-    ring_attn_bf16_pair_kernel<D><<<static_cast<unsigned>(tiles / 2), kThreads2, smem, stream>>>(mq, mk, mv, prm);
-    RA_LAUNCH_CHECK("ring_attn_bf16_pair_kernel");
+    attn_pair_kernel<D, RingPolicy><<<static_cast<unsigned>(tiles / 2), kThreads2, smem, stream>>>(mq, mk, mv, prm);
+    RA_LAUNCH_CHECK("attn_pair_kernel<RingPolicy>");
     return RA_OK;
   }
   const size_t smem = sizeof(Smem<D>) + 1024;
@@ -776,7 +541,7 @@ extern "C" ra_status ra_ring_attn_fwd_ex(const void* q, const void* k, const voi
   Params prm;
   prm.B = B; prm.Hq = Hq; prm.Hkv = Hkv; prm.S = S; prm.N = n_ranks; prm.c = S / (2 * n_ranks);
   prm.nt = static_cast<int>(ra::ceil_div(prm.c, BM));
-  prm.causal = causal ? 1 : 0; prm.layout = layout; prm.group = Hq / Hkv;
+  prm.causal = causal ? 1 : 0; prm.layout = layout; prm.group = Hq / Hkv; prm.d = d;
   prm.scale_log2 = sc * 1.4426950408889634f;
   prm.o = static_cast<__nv_bfloat16*>(o); prm.lse = lse;
   prm.wait_limit = ra::wait_limit();

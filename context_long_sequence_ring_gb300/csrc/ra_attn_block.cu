@@ -6,7 +6,7 @@
 // folded in with the blockwise decomposition); vLLM-Ascend developer guide
 // "Context Parallel (CP)", chunked prefill (a maximum amount of KV per round,
 // attention and online-softmax update segment after segment).
-#include "ra_attn_tc.cuh"
+#include "ra_attn_pair.cuh"
 
 RA_DEFINE_ERROR_FETCH(fetch_error_attn_block)
 
@@ -18,10 +18,11 @@ using namespace ra::sm100;
 // positions k_pos0 + j (one K/V block of a ring step, or one segment of a
 // chunked prefill), causal by absolute position.  Output: the partial's O
 // (fp32, already normalised by its own row sum) and LSE, to be combined with
-// other partials by the LSE merge.  One CTA per (128-row query tile, query
-// head); the pipeline is that of the one-head ring kernel (TMA producer, one
-// MMA thread, a softmax warpgroup, P via shared memory, double-buffered S).
-// A row with no visible key gets O = 0 and LSE = -inf.
+// other partials by the LSE merge.  A row with no visible key gets O = 0 and
+// LSE = -inf.  Even GQA groups run the two-head kernel with BlockPolicy; odd
+// groups run the one-head kernel below: one CTA per (128-row query tile, query
+// head), with the pipeline of the one-head ring kernel (TMA producer, one MMA
+// thread, a softmax warpgroup, P via shared memory, double-buffered S).
 // ===========================================================================
 struct BlockParams {
   int Tq, Tk, Hq, Hkv, group, causal;
@@ -42,6 +43,78 @@ __device__ __forceinline__ int block_n_kv(const BlockParams& p, int qt) {
   const long long seen = (last_q - p.k_pos0) / BN + 1;
   return static_cast<int>(seen < ntk ? seen : ntk);
 }
+
+// Causal mask of key tile kt for query row `row` of tile qt, by absolute position.
+__device__ __forceinline__ void block_mask(const BlockParams& p, int qt, int kt, int row, int& col_lim,
+                                           bool& masked) {
+  const int kv_valid = min(BN, p.Tk - kt * BN);
+  col_lim = kv_valid;
+  masked = kv_valid < BN;
+  if (p.causal) {
+    const long long qpos = p.q_pos0 + static_cast<long long>(qt) * BM + row;
+    const long long kpos0 = p.k_pos0 + static_cast<long long>(kt) * BN;
+    const long long vis = qpos - kpos0 + 1;   // keys of this tile visible to the row
+    col_lim = vis < 0 ? 0 : (vis > kv_valid ? kv_valid : static_cast<int>(vis));
+    masked = masked || kpos0 + kv_valid - 1 > p.q_pos0 + static_cast<long long>(qt) * BM;
+  }
+}
+
+// Block schedule for the two-head kernel (GQA groups of even size): one query
+// tile and a head pair per CTA, key tiles 0..n-1 of the block in order, fp32
+// partial output.
+template <int D>
+struct BlockPolicy {
+  using Args = BlockParams;
+  struct KvPos {
+    int kt;
+    int32_t row;
+  };
+  const BlockParams& p;
+  int qt, h0, g, nkv;
+  __device__ BlockPolicy(const BlockParams& a, int idx) : p(a) {
+    const int pairs = a.Hq / 2;
+    h0 = 2 * (idx % pairs);
+    qt = idx / pairs;
+    g = h0 / a.group;
+    nkv = block_n_kv(a, qt);
+  }
+  __device__ int tiles() const { return nkv > 0 ? 1 : 0; }
+  __device__ int hq0() const { return h0; }
+  __device__ int kvh() const { return g; }
+  __device__ void set_tile(int) {}
+  __device__ int32_t q_row() const { return qt * BM; }
+  __device__ int q_valid() const { return min(BM, p.Tq - qt * BM); }
+  __device__ int n_kv() const { return nkv; }
+  __device__ void kv_begin(KvPos& k) const { k.kt = -1; }
+  __device__ bool kv_next(KvPos& k) const {
+    if (++k.kt >= nkv) return false;
+    k.row = k.kt * BN;
+    return true;
+  }
+  __device__ void mask(const KvPos& k, int row, int& col_lim, bool& masked) const {
+    block_mask(p, qt, k.kt, row, col_lim, masked);
+  }
+  __device__ void store_o(int h, int row, int col0, const uint32_t (&o)[32], float inv_l) const {
+    float* dst = p.o + (static_cast<int64_t>(qt * BM + row) * p.Hq + h0 + h) * D + col0;
+#pragma unroll
+    for (int i = 0; i < 32; i += 4)
+      *reinterpret_cast<float4*>(dst + i) =
+          make_float4(__uint_as_float(o[i]) * inv_l, __uint_as_float(o[i + 1]) * inv_l,
+                      __uint_as_float(o[i + 2]) * inv_l, __uint_as_float(o[i + 3]) * inv_l);
+  }
+  __device__ void store_lse(int h, int row, float lse) const {
+    p.lse[static_cast<int64_t>(qt * BM + row) * p.Hq + h0 + h] = lse;
+  }
+  __device__ void write_empty(int tid, int nthreads) const {
+    const int qv = q_valid();
+    for (int i = tid; i < 2 * qv * D; i += nthreads) {
+      const int h = i / (qv * D), r = (i / D) % qv, e = i % D;
+      const int64_t at = static_cast<int64_t>(qt * BM + r) * p.Hq + h0 + h;
+      p.o[at * D + e] = 0.f;
+      if (e == 0) p.lse[at] = -CUDART_INF_F;
+    }
+  }
+};
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -182,20 +255,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = quarter * 32 + lane;
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const uint32_t p_base = smem_u32(sm.p);
-    const long long qpos = p.q_pos0 + static_cast<long long>(qt) * BM + row;
     float m = -CUDART_INF_F, l = 0.f;
     bool ok = true;
     for (int j = 0; j < nkv; ++j) {
       const int sb = j & 1;
-      const int kv_valid = min(BN, p.Tk - j * BN);
-      const long long kpos0 = p.k_pos0 + static_cast<long long>(j) * BN;
-      int col_lim = kv_valid;
-      bool masked = kv_valid < BN;
-      if (p.causal) {
-        const long long vis = qpos - kpos0 + 1;   // keys of this tile visible to the row
-        col_lim = vis < 0 ? 0 : (vis > kv_valid ? kv_valid : static_cast<int>(vis));
-        masked = masked || kpos0 + kv_valid - 1 > p.q_pos0 + static_cast<long long>(qt) * BM;
-      }
+      int col_lim;
+      bool masked;
+      block_mask(p, qt, j, row, col_lim, masked);
       if (!(ok = mbar_wait(smem_u32(&sm.s_full[sb]), (j >> 1) & 1, abort_flag, lim, 320))) break;
       tc_fence_after();
       uint32_t pk[BN / 2];
@@ -268,6 +334,15 @@ ra_status launch_block(const void* q, const void* k, const void* v, const BlockP
   if ((st = make_map(&mq, q, D, bp.Hq, bp.Tq)) != RA_OK) return st;
   if ((st = make_map(&mk, k, D, bp.Hkv, bp.Tk)) != RA_OK) return st;
   if ((st = make_map(&mv, v, D, bp.Hkv, bp.Tk)) != RA_OK) return st;
+  if (bp.group % 2 == 0) {  // two query heads of one GQA group per CTA
+    const size_t smem = sizeof(Smem2<D>) + 1024;
+    RA_CUDA_TRY(cudaFuncSetAttribute(attn_pair_kernel<D, BlockPolicy<D>>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(smem)));
+    const int64_t grid = ra::ceil_div(bp.Tq, BM) * (bp.Hq / 2);
+    attn_pair_kernel<D, BlockPolicy<D>><<<static_cast<unsigned>(grid), kThreads2, smem, stream>>>(mq, mk, mv, bp);
+    RA_LAUNCH_CHECK("attn_pair_kernel<BlockPolicy>");
+    return RA_OK;
+  }
   const size_t smem = sizeof(Smem<D>) + 1024;
   RA_CUDA_TRY(cudaFuncSetAttribute(block_attn_bf16_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    static_cast<int>(smem)));

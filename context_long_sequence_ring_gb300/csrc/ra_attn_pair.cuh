@@ -1,0 +1,301 @@
+// Two-head tcgen05 attention pipeline shared by the ring-order kernel and the
+// block-partial kernel.  A schedule policy Pol supplies (device side):
+//   Pol(const Args&, int item)          decode the CTA's work item
+//   int tiles()                          query tiles of the CTA (1 or 2)
+//   int hq0(), kvh()                     the two query heads hq0, hq0+1 and their K/V head
+//   void set_tile(int ti)                select query tile ti
+//   int32_t q_row(); int q_valid()       TMA row of its first query, valid rows
+//   int n_kv()                           K/V tiles the query tile meets
+//   KvPos; kv_begin(KvPos&); bool kv_next(KvPos&)   those tiles in order (KvPos::row = TMA row)
+//   void mask(const KvPos&, int row, int& col_lim, bool& masked)
+//   void store_o(int h, int row, int col0, const uint32_t (&o)[32], float inv_l)
+//   void store_lse(int h, int row, float lse)
+//   void write_empty(int tid, int nthreads)   outputs of a CTA with no query tile to run (tiles() == 0)
+// and Args carries scale_log2 and wait_limit.
+#pragma once
+
+#include "ra_attn_tc.cuh"
+
+namespace {
+using namespace ra::sm100;
+
+// ===========================================================================
+// Two-head tcgen05 attention kernel, templated on a schedule policy: a CTA runs
+// two query heads that read the same K/V head (a GQA pair), so every K/V tile
+// TMA brings in feeds two score tiles.  The policy supplies the query tiles of
+// the CTA, the K/V tiles each one meets (and in which order), the causal mask
+// and where the output goes: ring order over virtual ranks for the ring kernel,
+// a plain key range at absolute positions for block partials.
+// Roles (384 threads): warp 0 TMA, warp 1 TMEM allocation + MMA issue, warps
+// 4..7 softmax of head 0, warps 8..11 softmax of head 1 (warps 2, 3 idle).
+// Tensor memory: S_h = cols [128h, 128h+128), O_h = cols [256+128h, ...).
+// P_h (bf16, two per column) overwrites the first 64 columns of S_h and is
+// the A operand of O_h += P_h V straight from tensor memory, so P never
+// touches shared memory.  One thread issues every MMA, in the order
+//   PV0_j, S0_{j+1}, PV1_j, S1_{j+1}
+// which staggers the two heads: each softmax warpgroup works while the tensor
+// core serves the other head (measured faster than one issuer per head).
+// tcgen05 operations of one thread execute in issue order, so S_h(j+1) may
+// overwrite the columns PV_h(j) reads.  A softmax warpgroup only waits for
+// the previous P.V when it must rescale O (lazy rescale, threshold 2^8).
+// ===========================================================================
+template <int D>
+struct __align__(1024) Smem2 {
+  uint8_t q[2][BM * D * 2];
+  uint8_t k[STAGES][BN * D * 2];
+  uint8_t v[STAGES][BN * D * 2];
+  uint64_t q_full, q_empty, k_full[STAGES], k_empty[STAGES], v_full[STAGES], v_empty[STAGES];
+  uint64_t s_full[2], p_full[2], pv_done[2], o_empty[2], drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+constexpr int kThreads2 = 384;
+
+template <int D, class Pol>
+__global__ void __launch_bounds__(kThreads2, 1)
+    attn_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ typename Pol::Args args) {
+  constexpr int SLABS = D / 64;
+  constexpr uint32_t kTileBytes = BM * D * 2;
+  constexpr uint32_t kIdescS = idesc_bf16_f32(BM, BN, 0, 0);
+  constexpr uint32_t kIdescO = idesc_bf16_f32(BM, D, 0, 1);
+
+  extern __shared__ uint8_t smem_raw[];
+  Smem2<D>& sm = *reinterpret_cast<Smem2<D>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  Pol pol(args, blockIdx.x);
+  const int n_tiles = pol.tiles();
+  if (n_tiles == 0) {  // nothing visible: the policy writes the empty result
+    pol.write_empty(threadIdx.x, blockDim.x);
+    return;
+  }
+  volatile int* abort_flag = &sm.abort_flag;
+  const long long lim = args.wait_limit;
+
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&sm.q_full), 1);
+    mbar_init(smem_u32(&sm.q_empty), 1);
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_u32(&sm.k_full[s]), 1);
+      mbar_init(smem_u32(&sm.k_empty[s]), 1);
+      mbar_init(smem_u32(&sm.v_full[s]), 1);
+      mbar_init(smem_u32(&sm.v_empty[s]), 1);
+    }
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(smem_u32(&sm.s_full[h]), 1);
+      mbar_init(smem_u32(&sm.p_full[h]), 128);
+      mbar_init(smem_u32(&sm.pv_done[h]), 1);
+      mbar_init(smem_u32(&sm.o_empty[h]), 128);
+    }
+    mbar_init(smem_u32(&sm.drain), 1);
+    sm.abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&sm.tmem_base), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+
+  if (warp == 0) {
+    // ============================================================ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      uint32_t kv_cnt = 0;
+      bool issued[STAGES] = {false, false};
+      uint32_t last_ph[STAGES] = {0, 0};
+      bool ok = true;
+      for (int ti = 0; ti < n_tiles && ok; ++ti) {
+        pol.set_tile(ti);
+        if (!(ok = mbar_wait(smem_u32(&sm.q_empty), (ti & 1) ^ 1, abort_flag, lim, 101))) break;
+        const uint32_t qb = smem_u32(&sm.q_full);
+        mbar_arrive_expect_tx(qb, 2 * kTileBytes);
+        const int32_t qrow = pol.q_row();
+        for (int h = 0; h < 2; ++h)
+          for (int s = 0; s < SLABS; ++s)
+            tma_load_3d(smem_u32(sm.q[h] + s * BM * 128), &tmQ, qb, 64 * s, pol.hq0() + h, qrow);
+        typename Pol::KvPos kp;
+        pol.kv_begin(kp);
+        while (pol.kv_next(kp)) {
+          const int st = kv_cnt % STAGES;
+          const uint32_t ph = (kv_cnt / STAGES) & 1;
+          const int32_t krow = kp.row;
+          if (!(ok = mbar_wait(smem_u32(&sm.k_empty[st]), ph ^ 1, abort_flag, lim, 102))) break;
+          mbar_arrive_expect_tx(smem_u32(&sm.k_full[st]), kTileBytes);
+          for (int s = 0; s < SLABS; ++s)
+            tma_load_3d(smem_u32(sm.k[st] + s * BN * 128), &tmK, smem_u32(&sm.k_full[st]), 64 * s, pol.kvh(), krow);
+          if (!(ok = mbar_wait(smem_u32(&sm.v_empty[st]), ph ^ 1, abort_flag, lim, 103))) break;
+          mbar_arrive_expect_tx(smem_u32(&sm.v_full[st]), kTileBytes);
+          for (int s = 0; s < SLABS; ++s)
+            tma_load_3d(smem_u32(sm.v[st] + s * BN * 128), &tmV, smem_u32(&sm.v_full[st]), 64 * s, pol.kvh(), krow);
+          issued[st] = true;
+          last_ph[st] = ph;
+          ++kv_cnt;
+        }
+      }
+      if (!ok) {
+        for (int s = 0; s < STAGES; ++s)
+          if (issued[s]) {
+            mbar_wait(smem_u32(&sm.k_full[s]), last_ph[s], abort_flag, 1 << 22, 0);
+            mbar_wait(smem_u32(&sm.v_full[s]), last_ph[s], abort_flag, 1 << 22, 0);
+          }
+      }
+    }
+  } else if (warp == 1) {
+    // ============================================================ MMA issuer
+    if (lane == 0) {
+      uint32_t kv_cnt = 0, pf_cnt[2] = {0, 0};
+      bool ok = true;
+      // descriptors of k-step 0; a k-step adds its byte offset / 16 to the start-address field
+      const uint64_t dq[2] = {desc_sw128(smem_u32(sm.q[0]), 16, 1024), desc_sw128(smem_u32(sm.q[1]), 16, 1024)};
+      const uint64_t dk[STAGES] = {desc_sw128(smem_u32(sm.k[0]), 16, 1024), desc_sw128(smem_u32(sm.k[1]), 16, 1024)};
+      const uint64_t dv[STAGES] = {desc_sw128(smem_u32(sm.v[0]), BN * 128, 1024),
+                                   desc_sw128(smem_u32(sm.v[1]), BN * 128, 1024)};
+      auto issue_s = [&](int h, int st) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off16 = ((kk >> 2) * (BM * 128) + (kk & 3) * 32) >> 4;
+          mma_bf16_ss(tmem + h * BN, dq[h] + off16, dk[st] + off16, kIdescS, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(smem_u32(&sm.s_full[h]));
+      };
+      auto issue_pv = [&](int h, int st, bool first) {
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)
+          mma_bf16_ts(tmem + kColO + h * D, tmem + h * BN + kk * 8, dv[st] + ((kk * 16 * 128) >> 4), kIdescO,
+                      (kk > 0 || !first) ? 1u : 0u);
+        mma_commit(smem_u32(&sm.pv_done[h]));
+      };
+      for (int ti = 0; ti < n_tiles && ok; ++ti) {
+        pol.set_tile(ti);
+        const int nkv = pol.n_kv();
+        if (!(ok = mbar_wait(smem_u32(&sm.q_full), ti & 1, abort_flag, lim, 110))) break;
+        // prologue: both score tiles of K/V tile 0
+        {
+          const int st = kv_cnt % STAGES;
+          if (!(ok = mbar_wait(smem_u32(&sm.k_full[st]), (kv_cnt / STAGES) & 1, abort_flag, lim, 111))) break;
+          tc_fence_after();
+          issue_s(0, st);
+          issue_s(1, st);
+          mma_commit(smem_u32(&sm.k_empty[st]));
+          if (nkv == 1) mma_commit(smem_u32(&sm.q_empty));
+        }
+        for (int j = 0; j < nkv && ok; ++j) {
+          const uint32_t c = kv_cnt + j;
+          const int st = c % STAGES;
+          const uint32_t ph = (c / STAGES) & 1;
+          const bool more = j + 1 < nkv;
+          const int st1 = (c + 1) % STAGES;
+          const uint32_t ph1 = ((c + 1) / STAGES) & 1;
+          // O_0 += P_0 V_j
+          if (!(ok = mbar_wait(smem_u32(&sm.p_full[0]), pf_cnt[0] & 1, abort_flag, lim, 112))) break;
+          ++pf_cnt[0];
+          if (!(ok = mbar_wait(smem_u32(&sm.v_full[st]), ph, abort_flag, lim, 113))) break;
+          if (j == 0 && !(ok = mbar_wait(smem_u32(&sm.o_empty[0]), (ti & 1) ^ 1, abort_flag, lim, 114))) break;
+          tc_fence_after();
+          issue_pv(0, st, j == 0);
+          // S_0 of tile j+1
+          if (more) {
+            if (!(ok = mbar_wait(smem_u32(&sm.k_full[st1]), ph1, abort_flag, lim, 115))) break;
+            tc_fence_after();
+            issue_s(0, st1);
+          }
+          // O_1 += P_1 V_j
+          if (!(ok = mbar_wait(smem_u32(&sm.p_full[1]), pf_cnt[1] & 1, abort_flag, lim, 116))) break;
+          ++pf_cnt[1];
+          if (j == 0 && !(ok = mbar_wait(smem_u32(&sm.o_empty[1]), (ti & 1) ^ 1, abort_flag, lim, 117))) break;
+          tc_fence_after();
+          issue_pv(1, st, j == 0);
+          mma_commit(smem_u32(&sm.v_empty[st]));
+          if (more) {
+            issue_s(1, st1);
+            mma_commit(smem_u32(&sm.k_empty[st1]));
+            if (j + 1 == nkv - 1) mma_commit(smem_u32(&sm.q_empty));
+          }
+        }
+        kv_cnt += nkv;
+      }
+      mma_commit(smem_u32(&sm.drain));
+      mbar_wait(smem_u32(&sm.drain), 0, abort_flag, ok ? lim : (1 << 22), 118);
+    }
+  } else if (warp >= 4) {
+    // ============================================================ softmax + epilogue (head h)
+    const int h = (warp - 4) >> 2;
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const uint32_t colS = h * BN, colO = kColO + h * D;
+    uint32_t s_cnt = 0, pv_base = 0;
+    bool ok = true;
+    for (int ti = 0; ti < n_tiles && ok; ++ti) {
+      pol.set_tile(ti);
+      const int q_valid = pol.q_valid();
+      const int nkv = pol.n_kv();
+      typename Pol::KvPos kp;
+      pol.kv_begin(kp);
+      float m = -CUDART_INF_F, l = 0.f;
+      for (int j = 0; j < nkv; ++j) {
+        pol.kv_next(kp);
+        if (!(ok = mbar_wait(smem_u32(&sm.s_full[h]), s_cnt & 1, abort_flag, lim, 120 + h))) break;
+        ++s_cnt;
+        tc_fence_after();
+        int col_lim;
+        bool masked;
+        pol.mask(kp, row, col_lim, masked);
+        uint32_t pk[BN / 2];
+        const float alpha = softmax_row(t_lane + colS, j, masked, col_lim, args.scale_log2, m, l, pk);
+        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+          // O_h must hold P_{j-1} V_{j-1} before it is rescaled
+          if (!(ok = mbar_wait(smem_u32(&sm.pv_done[h]), (pv_base + j - 1) & 1, abort_flag, lim, 124 + h))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int c4 = 0; c4 < D / 32; ++c4) {
+            uint32_t orr[32];
+            tmem_ld32(t_lane + colO + 32 * c4, orr);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
+            tmem_st32(t_lane + colO + 32 * c4, orr);
+          }
+        }
+        // P_h into the first 64 columns of S_h
+        tmem_st32(t_lane + colS, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
+        tmem_st32(t_lane + colS + 32, *reinterpret_cast<const uint32_t(*)[32]>(&pk[32]));
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(smem_u32(&sm.p_full[h]));
+      }
+      if (!ok) break;
+      // ---------------------------------------------------------- epilogue
+      if (!(ok = mbar_wait(smem_u32(&sm.pv_done[h]), (pv_base + nkv - 1) & 1, abort_flag, lim, 126 + h))) break;
+      pv_base += nkv;
+      tc_fence_after();
+      const float inv_l = l > 0.f ? 1.f / l : 0.f;
+      const bool row_ok = row < q_valid;
+#pragma unroll
+      for (int c4 = 0; c4 < D / 32; ++c4) {
+        uint32_t orr[32];
+        tmem_ld32(t_lane + colO + 32 * c4, orr);
+        tmem_wait_ld();
+        if (row_ok) pol.store_o(h, row, 32 * c4, orr, inv_l);
+      }
+      tc_fence_before();
+      mbar_arrive(smem_u32(&sm.o_empty[h]));
+      if (row_ok) pol.store_lse(h, row, l > 0.f ? (m + log2f(l)) * kLn2 : -CUDART_INF_F);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+
+}  // namespace
