@@ -95,7 +95,7 @@ __device__ __forceinline__ void tile_mask(const Sched& s, int qc, int qi, int kc
 }
 
 struct Params {
-  int B, Hq, Hkv, S, N, c, nt, causal, layout, group, d;
+  int B, Hq, Hkv, S, N, c, nt, causal, layout, group;
   float scale_log2;
   __nv_bfloat16* o;
   float* lse;
@@ -405,6 +405,7 @@ __device__ __forceinline__ Item2 decode_item2(const Params& p, int idx) {
 
 // Ring schedule: a mirrored pair of query tiles of one virtual rank, K/V tiles
 // in ring order, causal mask by original position, bf16 output.
+template <int D>
 struct RingPolicy {
   using Args = Params;
   struct KvPos {
@@ -439,7 +440,7 @@ struct RingPolicy {
   }
   __device__ void store_o(int h, int row, int col0, const uint32_t (&o)[32], float inv_l) const {
     const int64_t trow = token_row(p, item.b, qc, qi * BM + row);
-    __nv_bfloat16* dst = p.o + (trow * p.Hq + item.hq0 + h) * (p.d) + col0;
+    __nv_bfloat16* dst = p.o + (trow * p.Hq + item.hq0 + h) * D + col0;
 #pragma unroll
     for (int i = 0; i < 32; i += 8) {
       uint4 pk;
@@ -492,9 +493,10 @@ ra_status launch_bf16(const void* q, const void* k, const void* v, const Params&
   const int64_t tiles = static_cast<int64_t>(prm.B) * prm.Hq * prm.N * prm.nt;  // mirrored tile pairs x heads
   if (variant == 2) {
     const size_t smem = sizeof(Smem2<D>) + 1024;
-    RA_CUDA_TRY(cudaFuncSetAttribute(attn_pair_kernel<D, RingPolicy>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     static_cast<int>(smem)));
-    attn_pair_kernel<D, RingPolicy><<<static_cast<unsigned>(tiles / 2), kThreads2, smem, stream>>>(mq, mk, mv, prm);
+    RA_CUDA_TRY(cudaFuncSetAttribute(attn_pair_kernel<D, RingPolicy<D>>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)));
+    attn_pair_kernel<D, RingPolicy<D>><<<static_cast<unsigned>(tiles / 2), kThreads2, smem, stream>>>(mq, mk, mv,
+                                                                                                     prm);
     RA_LAUNCH_CHECK("attn_pair_kernel<RingPolicy>");
     return RA_OK;
   }
@@ -541,7 +543,7 @@ extern "C" ra_status ra_ring_attn_fwd_ex(const void* q, const void* k, const voi
   Params prm;
   prm.B = B; prm.Hq = Hq; prm.Hkv = Hkv; prm.S = S; prm.N = n_ranks; prm.c = S / (2 * n_ranks);
   prm.nt = static_cast<int>(ra::ceil_div(prm.c, BM));
-  prm.causal = causal ? 1 : 0; prm.layout = layout; prm.group = Hq / Hkv; prm.d = d;
+  prm.causal = causal ? 1 : 0; prm.layout = layout; prm.group = Hq / Hkv;
   prm.scale_log2 = sc * 1.4426950408889634f;
   prm.o = static_cast<__nv_bfloat16*>(o); prm.lse = lse;
   prm.wait_limit = ra::wait_limit();
