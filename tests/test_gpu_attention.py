@@ -66,6 +66,8 @@ def test_fp32_ragged_and_gqa(ra, S, N, causal, Hq, Hkv, d):
     (768, 4, 1, 2, 1, 64, True),       # d = 64, chunks of 96 (single ragged tile)
     (2048, 4, 1, 2, 2, 64, False),
     (16, 8, 1, 2, 2, 128, True),       # chunks of 1 token
+    (256, 1, 1, 4, 2, 128, True),      # one virtual rank: the ring is a single step
+    (384, 1, 2, 2, 2, 128, False),
 ])
 @pytest.mark.parametrize("variant", [1, 2])
 def test_bf16_parity_small(ra, S, N, B, Hq, Hkv, d, causal, variant):

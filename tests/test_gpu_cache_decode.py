@@ -254,3 +254,19 @@ def test_kv_gather_bad_block_is_reported(ra):
     k, v = ra.cp_kv_gather(kc, kc, bt, qsl, pos, 8, 2, 1)
     assert ra.device_status() == ra.RA_ERR_DEVICE_BOUNDS
     assert torch.equal(k[1].cpu(), torch.zeros_like(k[1].cpu()))
+
+
+def test_empty_inputs_launch_nothing(ra):
+    """Zero tokens / rows are valid and leave the outputs untouched."""
+    z32 = torch.zeros(0, dtype=torch.int32, device=DEV)
+    out = torch.zeros((8, 0), dtype=torch.int32, device=DEV)
+    ra.cp_slot_mapping(torch.zeros(2, dtype=torch.int32, device=DEV), z32,
+                       torch.zeros((1, 1), dtype=torch.int32, device=DEV), 128, 16, 2, 4, out=out)
+    kc = torch.zeros((8, 1, 1, 128, 128), dtype=torch.bfloat16, device=DEV)
+    kz = torch.zeros((0, 1, 128), dtype=torch.bfloat16, device=DEV)
+    ra.cp_kv_scatter(kz, kz, torch.zeros((8, 0), dtype=torch.int32, device=DEV), kc, kc)
+    y = ra.gather_rows(torch.ones((4, 3), device=DEV), z32)
+    assert y.shape == (0, 3)
+    perm, restore = ra.zigzag_partition([0, 0], 4)
+    assert perm.numel() == 0 and restore.numel() == 0
+    check_status(ra)
