@@ -27,6 +27,9 @@ primitive).  Sources, by page title and section:
   parallel (PCP)" / head-tail token partition (pad, split into 2*pcp parts,
   pair part i with part 2*pcp-1-i, restore index), and the decode sections
   (partial outputs and LSEs merged by a cp_lse_ag_out_rs-style update).
+* guijiagi.com tag page "Ring Attention", article on the evolution of
+  long-context techniques, section 1.2 "RoPE": the rotary position embedding
+  of query and key rows.
 
 Parity status of every function is recorded in its docstring; all are pinned
 by the ``-m "not gpu"`` tests (closed forms, hand-worked golden values,
@@ -37,6 +40,7 @@ from .attention import (full_attention, attention_rows, attention_block, segment
                         ring_attention, ring_partials, lse_merge, rank_chunks,
                         causal_pairs_per_rank, causal_tiles_per_rank)
 from .partition import zigzag_partition, gather_rows
+from .rope import rope_theta, rope_cos_sin, rotate_half, apply_rope, rope_gather
 from .kvcache import (cp_slot_mapping, cp_token_location, cp_kv_scatter, cp_kv_gather,
                       cp_decode, cp_decode_partials, decode_reference)
 
@@ -46,4 +50,5 @@ __all__ = [
     "lse_merge", "rank_chunks", "causal_pairs_per_rank", "causal_tiles_per_rank",
     "zigzag_partition", "gather_rows", "cp_slot_mapping", "cp_token_location",
     "cp_kv_scatter", "cp_kv_gather", "cp_decode", "cp_decode_partials", "decode_reference",
+    "rope_theta", "rope_cos_sin", "rotate_half", "apply_rope", "rope_gather",
 ]
