@@ -332,6 +332,7 @@ def run_ours(args, rank, world, dev):
     }
     line["next_segmented_prefill"] = measure_segmented(ra, dev)
     line["next_kv_reorg"] = measure_kv_reorg(ra, wl)
+    line["next_rope_prologue"] = measure_rope(ra, wl)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_rows)
     return line
@@ -359,6 +360,8 @@ def run_parts(args, dev):
         out["ring_attn_tflops"] = causal_flops(P["B"], P["Hq"], P["S"], P["d"]) / (out["ring_attn_kernel_ms"] * 1e-3) / 1e12
     if "decode" in parts:
         out["decode_merge_gbs"] = wl.decode_bytes()[0] / (out["decode_merge_ms"] * 1e-3) / 1e9
+    if "rope" in parts:
+        out["rope"] = measure_rope(ra, wl)
     print(json.dumps(out), flush=True)
 
 
@@ -421,6 +424,48 @@ def measure_kv_reorg(ra, wl, n_req=8, reps=5):
     gbs = nbytes / (ms * 1e-3) / 1e9
     return {"requests": n_req, "tokens": T, "ms": round(ms, 3), "gbs": round(gbs, 1),
             "frac_of_hbm": round(gbs / _peaks()["hbm"], 4)}
+
+
+def measure_rope(ra, wl, reps=5):
+    """RoPE prologue (the next scope row after the KV reorg): the prefill's Q and K rotated by
+    their positions while they are gathered to the zigzag layout, against the plain gather of the
+    same rows.  Timed alone with CUDA events; the partition comes from the last bench step."""
+    P = PREFILL
+    if "prefill" not in wl.parts:
+        return None
+    pos = torch.arange(P["S"], dtype=torch.int32, device=wl.dev).repeat(P["B"])
+
+    def rope():
+        ra.rope_gather(wl.q, pos, wl.perm, out=wl.qz)
+        ra.rope_gather(wl.k, pos, wl.perm, out=wl.kz)
+
+    def plain():
+        ra.gather_rows(wl.q, wl.perm, wl.qz)
+        ra.gather_rows(wl.k, wl.perm, wl.kz)
+
+    res = {}
+    for name, fn in (("rope", rope), ("plain", plain)):
+        for _ in range(2):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        res[name] = e0.elapsed_time(e1) / reps
+    if ra.device_status() != 0:
+        raise RuntimeError("device status after the RoPE prologue: %s" % ra.last_error())
+    rows = P["B"] * P["S"]
+    G = int(wl.perm.numel())
+    # Q and K rows read once and written once, plus the gather index and one position per row
+    nbytes = (rows + G) * (P["Hq"] + P["Hkv"]) * P["d"] * 2 + 2 * (G * 4 + rows * 4)
+    gbs = nbytes / (res["rope"] * 1e-3) / 1e9
+    return {"tensors": "Q [%d, %d, %d] and K [%d, %d, %d] bf16, base 10000" % (rows, P["Hq"], P["d"], rows, P["Hkv"],
+                                                                               P["d"]),
+            "ms": round(res["rope"], 4), "gbs": round(gbs, 1), "frac_of_hbm": round(gbs / _peaks()["hbm"], 4),
+            "plain_gather_ms": round(res["plain"], 4), "vs_plain_gather": round(res["rope"] / res["plain"], 3)}
 
 
 # ---------------------------------------------------------------------------- oracle arm
@@ -516,8 +561,8 @@ def main():
     ap.add_argument("--cpu-rows", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--parts", default="all",
-                    help="'all' for the benchmark line, else 'prefill', 'decode' or 'prefill,decode' "
-                         "to run only those parts (profiler captures)")
+                    help="'all' for the benchmark line, else a comma list of 'prefill', 'decode' and "
+                         "'rope' (the RoPE prologue, needs 'prefill') to run only those parts (profiler captures)")
     ap.add_argument("--prefill-seq", type=int, default=None, help="override S of the prefill (multiple of 2N)")
     ap.add_argument("--decode-requests", type=int, default=None, help="override the number of decode requests")
     args = ap.parse_args()

@@ -20,7 +20,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libringattn.so")
 
-SOURCES = ["ra_api.cu", "ra_cache.cu", "ra_decode.cu", "ra_attn_f32.cu", "ra_attn_bf16.cu", "ra_attn_block.cu"]
+SOURCES = ["ra_api.cu", "ra_cache.cu", "ra_decode.cu", "ra_attn_f32.cu", "ra_attn_bf16.cu", "ra_attn_block.cu",
+           "ra_rope.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", INCLUDE, "-I", CSRC]

@@ -45,11 +45,12 @@ extern "C" ra_status ra_device_status(ra_stream stream) {
   cudaError_t e = cudaStreamSynchronize(stream);
   if (e != cudaSuccess) return ra::cuda_status(e, "cudaStreamSynchronize");
   int (*fetch[])(int*) = {ra::fetch_error_api, ra::fetch_error_cache, ra::fetch_error_decode,
-                          ra::fetch_error_attn_f32, ra::fetch_error_attn_bf16, ra::fetch_error_attn_block};
+                          ra::fetch_error_attn_f32, ra::fetch_error_attn_bf16, ra::fetch_error_attn_block,
+                          ra::fetch_error_rope};
   const char* names[] = {"partition/gather", "kv cache", "decode/merge", "attention fp32",
-                         "ring attention bf16", "block attention bf16"};
+                         "ring attention bf16", "block attention bf16", "rope gather"};
   ra_status first = RA_OK;
-  for (int i = 0; i < 6; ++i) {
+  for (int i = 0; i < 7; ++i) {
     int where = 0;
     int s = fetch[i](&where);
     if (s < 0) return ra::fail(RA_ERR_CUDA, "reading the device error word failed");

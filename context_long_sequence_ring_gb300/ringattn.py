@@ -28,6 +28,7 @@ SIGNATURES = {
     "ra_device_status": [_vp],
     "ra_zigzag_partition": [_c.POINTER(_i64), _i32, _i32, _vp, _vp, _c.POINTER(_i64), _c.POINTER(_i64), _vp],
     "ra_gather_rows": [_vp, _i64, _vp, _vp, _i64, _i64, _vp],
+    "ra_rope_gather": [_vp, _i64, _i32, _i32, _c.c_int, _vp, _i64, _vp, _c.c_double, _vp, _vp],
     "ra_ring_attn_fwd": [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _c.c_int, _i32, _i32, _f32,
                          _c.c_int, _vp],
     "ra_ring_attn_fwd_ex": [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _c.c_int, _i32, _i32, _f32,
@@ -149,6 +150,27 @@ def gather_rows(src: torch.Tensor, idx: torch.Tensor, out: Optional[torch.Tensor
         out = torch.empty((rows,) + tuple(src.shape[1:]), dtype=src.dtype, device=src.device)
     row_bytes = src[0].numel() * src.element_size() if src.shape[0] > 0 else 0
     _check(lib().ra_gather_rows(_ptr(src), src.shape[0], _ptr(idx), _ptr(out), rows, row_bytes, _stream()))
+    return out
+
+
+def rope_gather(src: torch.Tensor, positions: torch.Tensor, idx: Optional[torch.Tensor] = None,
+                base: float = 10000.0, out: Optional[torch.Tensor] = None):
+    """Rotary position embedding fused with a row gather: out[r] = RoPE(src[idx[r]],
+    positions[idx[r]]), zero rows where idx < 0.  src [rows, H, d]; positions int32, one per
+    source row.  Without idx the rows keep their order (out may be src: in place)."""
+    _need_cuda(src, positions, idx, out)
+    if src.dim() != 3:
+        raise ValueError("src must be [rows, H, d]")
+    if positions.dtype != torch.int32 or (idx is not None and idx.dtype != torch.int32):
+        raise ValueError("positions and idx must be int32")
+    if positions.numel() != src.shape[0]:
+        raise ValueError("one position per source row")
+    rows = idx.numel() if idx is not None else src.shape[0]
+    if out is None:
+        out = torch.empty((rows,) + tuple(src.shape[1:]), dtype=src.dtype, device=src.device)
+    _check(lib().ra_rope_gather(_ptr(src), src.shape[0], src.shape[1], src.shape[2], _dt(src),
+                                _ptr(idx) if idx is not None else None, rows, _ptr(positions), float(base),
+                                _ptr(out), _stream()))
     return out
 
 

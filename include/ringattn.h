@@ -103,6 +103,37 @@ ra_status ra_gather_rows(const void* src, int64_t src_rows, const int32_t* idx, 
                          int64_t rows, int64_t row_bytes, ra_stream stream);
 
 /* ------------------------------------------------------------------------
+ * ra_rope_gather -- rotary position embedding of Q or K rows, fused with the
+ * row gather of the zigzag permute:
+ *   dst[r] = RoPE(src[idx[r]], positions[idx[r]])   (a zero row where idx[r] < 0)
+ * Source: guijiagi.com tag page "Ring Attention", article on the evolution of
+ * long-context techniques, section 1.2 "RoPE": RoPE(x, m) = x e^{i m theta},
+ * theta_i = base^(-2i/d) (i = 0 .. d/2-1), real form
+ * x*cos + rotate_half(x)*sin, rotate_half(x1, x2) = (-x2, x1): component j and
+ * component j + d/2 of each head are the real and imaginary parts of the j-th
+ * complex number, turned by the angle m * theta_j.
+ *
+ * src        device [src_rows, H, d] of dt (RA_BF16 or RA_F32), 16-byte aligned.
+ * idx        device int32 [rows] (e.g. the perm of ra_zigzag_partition), or
+ *            NULL for the identity (then rows == src_rows, and dst may be src
+ *            itself: the rotation is done in place).
+ * positions  device int32 [src_rows]: the position m of each SOURCE row (its
+ *            index inside its own sequence), in [0, 2^24).
+ * base       the RoPE base (10000 on the page), finite and > 1.
+ * dst        device [rows, H, d] of dt out, 16-byte aligned; must not overlap
+ *            src when idx is given.
+ * d must be a multiple of 16 (bf16) or 8 (fp32), at most 256.  The rotation
+ * is computed in fp32 (angles reduced to turns with an error-free product, so
+ * their error does not grow with the position) and rounded once to dt.
+ * An idx >= src_rows or a position outside [0, 2^24) is a device-side bounds
+ * error (RA_ERR_DEVICE_BOUNDS recorded; the row is zero-filled, resp. the
+ * position taken as 0).
+ * ---------------------------------------------------------------------- */
+ra_status ra_rope_gather(const void* src, int64_t src_rows, int32_t H, int32_t d, ra_dtype dt,
+                         const int32_t* idx, int64_t rows, const int32_t* positions, double base,
+                         void* dst, ra_stream stream);
+
+/* ------------------------------------------------------------------------
  * ra_ring_attn_fwd -- causal or full GQA attention forward computed in ring
  * order over N virtual context-parallel ranks with blockwise online softmax.
  * Sources: "Parallelism-CP" diagram (Q/K/V split along the sequence, K/V

@@ -110,6 +110,26 @@ def test_merge_validation(ra):
     assert _call(ra, "ra_lse_merge", p, p, 2, 4, 2, 6, p, 0, p, None) == ra.RA_ERR_UNSUPPORTED
 
 
+def test_rope_gather_validation(ra):
+    p = ctypes.c_void_p(1 << 20)
+    q = ctypes.c_void_p(1 << 24)
+
+    def run(src=p, H=4, d=128, dt=1, idx=p, rows=8, pos=p, base=10000.0, dst=q, src_rows=8):
+        return _call(ra, "ra_rope_gather", src, src_rows, H, d, dt, idx, rows, pos, ctypes.c_double(base), dst, None)
+
+    assert run(d=120) == ra.RA_ERR_INVALID_ARG and "multiple of 16" in ra.last_error()
+    assert run(d=264) == ra.RA_ERR_INVALID_ARG
+    assert run(d=12, dt=0) == ra.RA_ERR_INVALID_ARG and "multiple of 8" in ra.last_error()
+    assert run(base=1.0) == ra.RA_ERR_INVALID_ARG and "base" in ra.last_error()
+    assert run(base=float("inf")) == ra.RA_ERR_INVALID_ARG
+    assert run(dt=7) == ra.RA_ERR_INVALID_ARG
+    assert run(pos=None) == ra.RA_ERR_INVALID_ARG and "NULL" in ra.last_error()
+    assert run(dst=ctypes.c_void_p((1 << 20) + 1024)) == ra.RA_ERR_INVALID_ARG and "overlap" in ra.last_error()
+    assert run(idx=None, rows=6) == ra.RA_ERR_INVALID_ARG
+    assert run(src=ctypes.c_void_p((1 << 20) + 8)) == ra.RA_ERR_INVALID_ARG and "aligned" in ra.last_error()
+    assert run(rows=0) == ra.RA_OK          # nothing to do, nothing launched
+
+
 def test_product_path_has_no_oracle_or_fallback():
     pkg = os.path.join(ROOT, "context_long_sequence_ring_gb300")
     for f in glob.glob(os.path.join(pkg, "*.py")) + glob.glob(os.path.join(pkg, "csrc", "*")):
