@@ -267,6 +267,9 @@ def run_ours(args, rank, world, dev):
     prefill_ms = statistics.mean(e[0].elapsed_time(e[3]) for e in evs)
     decode_kernel_ms = statistics.mean(e[4].elapsed_time(e[5]) for e in evs)
     decode_ms = statistics.mean(e[3].elapsed_time(e[5]) for e in evs)
+    partition_gather_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    restore_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
+    slot_scatter_ms = statistics.mean(e[3].elapsed_time(e[4]) for e in evs)
     flops = causal_flops(P["B"], P["Hq"], P["S"], P["d"])
     dec_bytes, kv_bytes = wl.decode_bytes()
     pk = _peaks()
@@ -315,6 +318,8 @@ def run_ours(args, rank, world, dev):
             "ring_attn_tflops": round(attn_tflops, 1),
             "decode_merge_ms": round(decode_kernel_ms, 4), "decode_step_ms": round(decode_ms, 4),
             "decode_merge_gbs": round(dec_gbs, 1), "decode_kv_bytes": kv_bytes, "decode_alg_bytes": dec_bytes,
+            "partition_gather_ms": round(partition_gather_ms, 4), "restore_ms": round(restore_ms, 4),
+            "slot_mapping_scatter_ms": round(slot_scatter_ms, 4),
         },
         "roofline": {"bound": "tensor", "achieved": round(attn_tflops, 1), "peak": pk["bf16_sus"], "unit": "TFLOP/s",
                      "frac": round(attn_tflops / pk["bf16_sus"], 4), "traffic": _traffic("ring_attn_bf16"),
@@ -333,6 +338,7 @@ def run_ours(args, rank, world, dev):
     line["next_segmented_prefill"] = measure_segmented(ra, dev)
     line["next_kv_reorg"] = measure_kv_reorg(ra, wl)
     line["next_rope_prologue"] = measure_rope(ra, wl)
+    line["merge_stress"] = measure_merge(ra, dev)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_rows)
     return line
@@ -424,6 +430,37 @@ def measure_kv_reorg(ra, wl, n_req=8, reps=5):
     gbs = nbytes / (ms * 1e-3) / 1e9
     return {"requests": n_req, "tokens": T, "ms": round(ms, 3), "gbs": round(gbs, 1),
             "frac_of_hbm": round(gbs / _peaks()["hbm"], 4)}
+
+
+MERGE = dict(P=8, T=32768, H=32, d=128, seed=7)
+
+
+def measure_merge(ra, dev, reps=10):
+    """The LSE merge on its own at a size where it is HBM-bound: P fp32 partials of [T, H, d]
+    (4.3 GB read) merged into a bf16 O and an fp32 LSE.  Timed with CUDA events."""
+    M = MERGE
+    P, T, H, d = M["P"], M["T"], M["H"], M["d"]
+    tab = I.normal_table(torch.float32)
+    o_parts = ra.synth_fill(I.tensor_key(M["seed"], 0), tab, (P, T, H, d), dev)
+    lse_parts = ra.synth_fill(I.tensor_key(M["seed"], 1), tab, (P, T, H), dev)
+    o = torch.empty((T, H, d), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((T, H), dtype=torch.float32, device=dev)
+    for _ in range(2):
+        ra.lse_merge(o_parts, lse_parts, o=o, lse=lse)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        ra.lse_merge(o_parts, lse_parts, o=o, lse=lse)
+    e1.record()
+    torch.cuda.synchronize()
+    if ra.device_status() != 0:
+        raise RuntimeError("device status after the merge stress: %s" % ra.last_error())
+    ms = e0.elapsed_time(e1) / reps
+    nbytes = P * T * H * (d + 1) * 4 + T * H * (d * 2 + 4)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    del o_parts, lse_parts
+    return {"config": M, "ms": round(ms, 4), "gbs": round(gbs, 1), "frac_of_hbm": round(gbs / _peaks()["hbm"], 4)}
 
 
 def measure_rope(ra, wl, reps=5):

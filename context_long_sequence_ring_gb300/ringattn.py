@@ -243,14 +243,17 @@ def segmented_prefill_fwd(q, k, v, q_pos0: int, seg_tokens: int, causal: bool = 
     return o, lse
 
 
-def lse_merge(o_parts, lse_parts, out_dtype=torch.float32):
-    """Merge partials o_parts [P, T, H, d] fp32 with lse_parts [P, T, H] -> (O [T, H, d], LSE [T, H])."""
-    _need_cuda(o_parts, lse_parts)
+def lse_merge(o_parts, lse_parts, out_dtype=torch.float32, o=None, lse=None):
+    """Merge partials o_parts [P, T, H, d] fp32 with lse_parts [P, T, H] -> (O [T, H, d], LSE [T, H]).
+    O takes out_dtype, or the dtype of a given ``o``."""
+    _need_cuda(o_parts, lse_parts, o, lse)
     P, T, H, d = o_parts.shape
-    o = torch.empty((T, H, d), dtype=out_dtype, device=o_parts.device)
-    lse = torch.empty((T, H), dtype=torch.float32, device=o_parts.device)
+    if o is None:
+        o = torch.empty((T, H, d), dtype=out_dtype, device=o_parts.device)
+    if lse is None:
+        lse = torch.empty((T, H), dtype=torch.float32, device=o_parts.device)
     _check(lib().ra_lse_merge(_ptr(o_parts), _ptr(lse_parts), P, T, H, d, _ptr(o),
-                              RA_BF16 if out_dtype == torch.bfloat16 else RA_F32, _ptr(lse), _stream()))
+                              RA_BF16 if o.dtype == torch.bfloat16 else RA_F32, _ptr(lse), _stream()))
     return o, lse
 
 
