@@ -105,45 +105,66 @@ __device__ __forceinline__ void chunk_exp_pack(const uint32_t (&x)[32], uint64_t
   }
 }
 
+// Columns [c0, c0+32) of a score row at or past col_lim become -inf (masked).
+__device__ __forceinline__ void chunk_mask(uint32_t (&x)[32], int c0, int col_lim) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i)
+    if (c0 + i >= col_lim) x[i] = __float_as_uint(-CUDART_INF_F);
+}
+
+// Largest sum of one 32-column chunk of p = 2^(s*scale - m) that keeps the
+// stale reference m: every p of the chunk is then at most 2^8, the bound the
+// row-max test held P to (a looser 2^12 measured larger O errors on sharp
+// softmaxes for half a percent of speed).
+constexpr float kChunkSumLimit = 256.f;
+
 // One online-softmax step for the score row at tensor-memory address s_addr
 // (BN fp32 columns, raw Q.K^T): fills pk with P in bf16 pairs and updates the
 // running max m (log2 units) and sum l.  Returns the factor O must be scaled by
 // (1 when unchanged).
 //
-// After the first K/V tile the row is read once, 32 columns at a time, with the
-// running max as reference: the exps start before the whole row is seen.  If
-// any row of the warp finds a score above max + 8 (log2), the warp falls back
-// to two passes (max, then exps) and the rows that grew move their reference.
-// The stale reference is exact because l and O always share it; 2^8 bounds P.
+// After the first K/V tile the row is read once, 32 columns at a time, and the
+// exps are taken at once against the running max, before the whole row is
+// seen.  The chunk's own sum of p then decides whether that reference still
+// holds: while it stays at most 2^8 every p is bounded by 2^8 and nothing
+// needs rescaling (the stale reference is exact because l and O always share
+// it).  This test costs three adds per chunk where a row max would cost a
+// reduction over all 32 scores.  If any row of the warp exceeds it (or has no
+// reference yet), the warp falls back to two passes (max, then exps) over the
+// scores, which are still in tensor memory, and rows whose max grew by more
+// than 2^8 move their reference.
 template <int NP>
 __device__ __forceinline__ float softmax_row(uint32_t s_addr, int j, bool masked, int col_lim, float scale,
                                              float& m, float& l, uint32_t (&pk)[NP]) {
   constexpr int NCOL = 2 * NP;
   const uint64_t sc2 = f2pack(scale, scale);
   if (j > 0) {
-    const float thr = (m + 8.f) / scale;   // raw-score threshold of a rescale
     const uint64_t negm2 = f2pack(-m, -m);
-    uint64_t acc0 = f2pack(0.f, 0.f), acc1 = acc0;
-    bool grow = false;
+    bool grow = __any_sync(0xffffffffu, m == -CUDART_INF_F);   // no reference yet: -inf - -inf is NaN
+    float lsum = 0.f;
     // the load of chunk c+1 is in flight while chunk c is processed
     uint32_t xa[32], xb[32];
     tmem_ld32(s_addr, xa);
     tmem_wait_ld();
 #pragma unroll
     for (int c = 0; c < NCOL / 32; ++c) {
+      if (grow) break;
       uint32_t (&x)[32] = (c & 1) ? xb : xa;
       uint32_t (&y)[32] = (c & 1) ? xa : xb;
       if (c + 1 < NCOL / 32) tmem_ld32(s_addr + 32 * (c + 1), y);
-      const float cm = chunk_mask_max(x, 32 * c, masked, col_lim);
-      if (__any_sync(0xffffffffu, cm > thr)) { grow = true; tmem_wait_ld(); break; }
+      if (masked) chunk_mask(x, 32 * c, col_lim);
+      uint64_t acc0 = f2pack(0.f, 0.f), acc1 = acc0;
       chunk_exp_pack(x, sc2, negm2, acc0, acc1, &pk[16 * c]);
-      if (c + 1 < NCOL / 32) tmem_wait_ld();
-    }
-    if (!grow) {
       float a0, a1, b0, b1;
       f2unpack(acc0, a0, a1);
       f2unpack(acc1, b0, b1);
-      l += (a0 + a1) + (b0 + b1);
+      const float cs = (a0 + a1) + (b0 + b1);
+      if (__any_sync(0xffffffffu, !(cs <= kChunkSumLimit))) { grow = true; tmem_wait_ld(); break; }
+      lsum += cs;
+      if (c + 1 < NCOL / 32) tmem_wait_ld();
+    }
+    if (!grow) {
+      l += lsum;
       return 1.f;
     }
   }
@@ -168,7 +189,7 @@ __device__ __forceinline__ float softmax_row(uint32_t s_addr, int j, bool masked
     uint32_t x[32];
     tmem_ld32(s_addr + 32 * c, x);
     tmem_wait_ld();
-    chunk_mask_max(x, 32 * c, masked, col_lim);
+    if (masked) chunk_mask(x, 32 * c, col_lim);
     chunk_exp_pack(x, sc2, negm2, acc0, acc1, &pk[16 * c]);
   }
   float a0, a1, b0, b1;

@@ -78,6 +78,28 @@ def test_bf16_parity_small(ra, S, N, B, Hq, Hkv, d, causal, variant):
     assert_parity(o, O, lse, L, torch.bfloat16, "bf16 v%d S=%d N=%d" % (variant, S, N))
 
 
+@pytest.mark.parametrize("case", ["sharp_scale", "growing_keys"])
+@pytest.mark.parametrize("variant", [1, 2])
+def test_bf16_rescale_paths(ra, case, variant):
+    """Inputs that make the running max grow inside and across K/V tiles, so the lazy
+    reference fails its check often: the two-pass fallback and the O rescale in tensor
+    memory both run.  sharp_scale: softmax scale 0.5 (scores of std ~5.7); growing_keys:
+    key rows scaled by 1 + 4 * position / S, so later tiles keep exceeding the reference."""
+    B, S, Hq, Hkv, d, N = 1, 1536, 4, 2, 128, 3
+    q, k, v = I.prefill_inputs(17, B, S, Hq, Hkv, d, torch.bfloat16)
+    scale = None
+    if case == "sharp_scale":
+        scale = 0.5
+    else:
+        grow = 1.0 + 4.0 * torch.arange(S, dtype=torch.float32) / S
+        k = (k.float() * grow[:, None, None]).to(torch.bfloat16)
+    dev = torch.device("cuda")
+    o, lse = ra.ring_attn_fwd(q.to(dev), k.to(dev), v.to(dev), True, N, B=B, scale=scale, variant=variant)
+    check_status(ra)
+    O, L = oracle.full_attention(q, k, v, True, scale=scale)
+    assert_parity(o, O, lse, L, torch.bfloat16, "%s v%d" % (case, variant))
+
+
 @pytest.mark.parametrize("other", [2])
 def test_bf16_variants_agree(ra, other):
     B, S, Hq, Hkv, d, N = 1, 2560, 8, 2, 128, 5
