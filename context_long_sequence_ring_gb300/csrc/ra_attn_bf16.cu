@@ -96,6 +96,7 @@ __device__ __forceinline__ void tile_mask(const Sched& s, int qc, int qi, int kc
 
 struct Params {
   int B, Hq, Hkv, S, N, c, nt, causal, layout, group;
+  int ntp, mirrored;  // adjacent-tile schedule: tile pairs per chunk, mirrored pairs per CTA
   float scale_log2;
   __nv_bfloat16* o;
   float* lse;
@@ -420,14 +421,14 @@ struct RingPolicy {
   __device__ RingPolicy(const Params& a, int idx)
       : p(a), item(decode_item2(a, idx)), sch{a.N, a.c, a.nt, a.causal, BN, a.nt}, qc(0), qi(0) {}
   __device__ int tiles() const { return 2; }
-  __device__ int hq0() const { return item.hq0; }
   __device__ int kvh() const { return item.g; }
   __device__ void set_tile(int ti) {
     const Item it1{item.b, item.hq0, item.g, item.r, item.j};
     tile_of(p, it1, ti, qc, qi);
   }
-  __device__ int32_t q_row() const { return static_cast<int32_t>(token_row(p, item.b, qc, qi * BM)); }
-  __device__ int q_valid() const { return min(BM, p.c - qi * BM); }
+  __device__ int q_head(int h) const { return item.hq0 + h; }
+  __device__ int32_t q_row(int) const { return static_cast<int32_t>(token_row(p, item.b, qc, qi * BM)); }
+  __device__ int q_valid(int) const { return min(BM, p.c - qi * BM); }
   __device__ int n_kv() const { return n_kv_tiles(sch, qc, qi); }
   __device__ void kv_begin(KvPos& k) const { k.it.init(sch, qc, qi); }
   __device__ bool kv_next(KvPos& k) const {
@@ -435,7 +436,7 @@ struct RingPolicy {
     k.row = static_cast<int32_t>(token_row(p, item.b, k.kc, k.kt * BN));
     return true;
   }
-  __device__ void mask(const KvPos& k, int row, int& col_lim, bool& masked) const {
+  __device__ void mask(const KvPos& k, int, int row, int& col_lim, bool& masked) const {
     tile_mask(sch, qc, qi, k.kc, k.kt, row, col_lim, masked);
   }
   __device__ void store_o(int h, int row, int col0, const uint32_t (&o)[32], float inv_l) const {
@@ -453,6 +454,80 @@ struct RingPolicy {
   }
   __device__ void store_lse(int h, int row, float lse) const {
     p.lse[token_row(p, item.b, qc, qi * BM + row) * p.Hq + item.hq0 + h] = lse;
+  }
+  __device__ void write_empty(int, int) const {}  // every ring query tile meets at least one key tile
+};
+
+// Adjacent-tile schedule, for any GQA group (odd ones and plain multi-head
+// attention included): one query head, with two adjacent 128-row query tiles
+// of one chunk, 2i and 2i+1, as the two slots.  The K/V tiles are those the
+// later tile meets, a superset of the earlier tile's under the causal mask
+// (one extra diagonal tile, fully masked for the earlier one), in ring order.
+// Mirrored: the CTA then runs the mirrored pair of chunk 2N-1-r, which evens
+// out the causal work as the head-pair schedule does with single tiles;
+// otherwise (small problems, to fill the SMs) one pair per CTA, the heaviest
+// pairs first.  A missing second tile (odd tile count) is an empty slot.
+template <int D>
+struct RingTilePolicy {
+  using Args = Params;
+  using KvPos = typename RingPolicy<D>::KvPos;
+  const Params& p;
+  Sched sch;
+  int b, hq, g, r, jp, qc, pr;
+  __device__ RingTilePolicy(const Params& a, int idx) : p(a), sch{a.N, a.c, a.nt, a.causal, BN, a.nt} {
+    const int hg = idx % a.group; idx /= a.group;
+    if (a.mirrored) {
+      jp = idx % a.ntp; idx /= a.ntp;
+      r = idx % a.N; idx /= a.N;
+      g = idx % a.Hkv; idx /= a.Hkv;
+      b = idx;
+    } else {
+      g = idx % a.Hkv; idx /= a.Hkv;
+      b = idx % a.B; idx /= a.B;
+      jp = a.ntp - 1 - idx % a.ntp; idx /= a.ntp;
+      r = 2 * a.N - 1 - idx;  // chunk index, last (heaviest) first
+    }
+    hq = g * a.group + hg;
+    qc = r;
+    pr = jp;
+  }
+  __device__ int tiles() const { return p.mirrored ? 2 : 1; }
+  __device__ int kvh() const { return g; }
+  __device__ void set_tile(int ti) {
+    if (ti == 0) { qc = r; pr = jp; }
+    else { qc = 2 * p.N - 1 - r; pr = p.ntp - 1 - jp; }
+  }
+  __device__ int q_head(int) const { return hq; }
+  __device__ int32_t q_row(int h) const {
+    return static_cast<int32_t>(token_row(p, b, qc, (2 * pr + h) * BM));
+  }
+  __device__ int q_valid(int h) const { return max(0, min(BM, p.c - (2 * pr + h) * BM)); }
+  __device__ int kv_tile() const { return min(2 * pr + 1, p.nt - 1); }
+  __device__ int n_kv() const { return n_kv_tiles(sch, qc, kv_tile()); }
+  __device__ void kv_begin(KvPos& k) const { k.it.init(sch, qc, kv_tile()); }
+  __device__ bool kv_next(KvPos& k) const {
+    if (!k.it.next(k.kc, k.kt)) return false;
+    k.row = static_cast<int32_t>(token_row(p, b, k.kc, k.kt * BN));
+    return true;
+  }
+  __device__ void mask(const KvPos& k, int h, int row, int& col_lim, bool& masked) const {
+    tile_mask(sch, qc, 2 * pr + h, k.kc, k.kt, row, col_lim, masked);
+  }
+  __device__ void store_o(int h, int row, int col0, const uint32_t (&o)[32], float inv_l) const {
+    const int64_t trow = token_row(p, b, qc, (2 * pr + h) * BM + row);
+    __nv_bfloat16* dst = p.o + (trow * p.Hq + hq) * D + col0;
+#pragma unroll
+    for (int i = 0; i < 32; i += 8) {
+      uint4 pk;
+      pk.x = f2_bf16x2(__uint_as_float(o[i]) * inv_l, __uint_as_float(o[i + 1]) * inv_l);
+      pk.y = f2_bf16x2(__uint_as_float(o[i + 2]) * inv_l, __uint_as_float(o[i + 3]) * inv_l);
+      pk.z = f2_bf16x2(__uint_as_float(o[i + 4]) * inv_l, __uint_as_float(o[i + 5]) * inv_l);
+      pk.w = f2_bf16x2(__uint_as_float(o[i + 6]) * inv_l, __uint_as_float(o[i + 7]) * inv_l);
+      *reinterpret_cast<uint4*>(dst + i) = pk;
+    }
+  }
+  __device__ void store_lse(int h, int row, float lse) const {
+    p.lse[token_row(p, b, qc, (2 * pr + h) * BM + row) * p.Hq + hq] = lse;
   }
   __device__ void write_empty(int, int) const {}  // every ring query tile meets at least one key tile
 };
@@ -500,6 +575,16 @@ ra_status launch_bf16(const void* q, const void* k, const void* v, const Params&
     RA_LAUNCH_CHECK("attn_pair_kernel<RingPolicy>");
     return RA_OK;
   }
+  if (variant == 3) {
+    const int64_t items = static_cast<int64_t>(prm.B) * prm.Hq * prm.ntp * (prm.mirrored ? prm.N : 2 * prm.N);
+    const size_t smem = sizeof(Smem2<D>) + 1024;
+    RA_CUDA_TRY(cudaFuncSetAttribute(attn_pair_kernel<D, RingTilePolicy<D>>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)));
+    attn_pair_kernel<D, RingTilePolicy<D>><<<static_cast<unsigned>(items), kThreads2, smem, stream>>>(mq, mk, mv,
+                                                                                                       prm);
+    RA_LAUNCH_CHECK("attn_pair_kernel<RingTilePolicy>");
+    return RA_OK;
+  }
   const size_t smem = sizeof(Smem<D>) + 1024;
   RA_CUDA_TRY(cudaFuncSetAttribute(ring_attn_bf16_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    static_cast<int>(smem)));
@@ -523,7 +608,7 @@ extern "C" ra_status ra_ring_attn_fwd_ex(const void* q, const void* k, const voi
                                          int32_t causal, int32_t n_ranks, float scale, ra_layout layout,
                                          int32_t variant, ra_stream stream) {
   ra::clear_error();
-  RA_REQUIRE(variant >= 0 && variant <= 2, "variant must be 0, 1 or 2");
+  RA_REQUIRE(variant >= 0 && variant <= 3, "variant must be 0, 1, 2 or 3");
   RA_REQUIRE(B >= 1 && Hq >= 1 && Hkv >= 1 && S >= 1, "B, Hq, Hkv, S must be >= 1");
   RA_REQUIRE(Hq % Hkv == 0, "Hq (%d) must be a multiple of Hkv (%d)", Hq, Hkv);
   RA_REQUIRE(n_ranks >= 1, "n_ranks must be >= 1 (got %d)", n_ranks);
@@ -549,8 +634,17 @@ extern "C" ra_status ra_ring_attn_fwd_ex(const void* q, const void* k, const voi
   prm.wait_limit = ra::wait_limit();
   const int64_t items = static_cast<int64_t>(B) * Hkv * n_ranks * prm.nt * prm.group;
   RA_REQUIRE(items < (int64_t(1) << 31), "too many work items");
-  if (variant == 0) variant = (prm.group % 2 == 0) ? 2 : 1;
-  RA_REQUIRE(variant == 1 || prm.group % 2 == 0, "the two-head variant needs an even Hq/Hkv");
+  prm.ntp = (prm.nt + 1) / 2;
+  prm.mirrored = 1;
+  if (variant == 0) variant = (prm.group % 2 == 0) ? 2 : 3;
+  RA_REQUIRE(variant != 2 || prm.group % 2 == 0, "the two-head variant needs an even Hq/Hkv");
+  if (variant == 3) {
+    // mirrored pairs halve the CTA count; keep them only while that still fills two waves
+    int dev = 0, sms = 0;
+    RA_CUDA_TRY(cudaGetDevice(&dev));
+    RA_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+    prm.mirrored = static_cast<int64_t>(B) * Hq * n_ranks * prm.ntp >= 2 * static_cast<int64_t>(sms) ? 1 : 0;
+  }
   if (d == 128) return launch_bf16<128>(q, k, v, prm, variant, stream);
   return launch_bf16<64>(q, k, v, prm, variant, stream);
 }

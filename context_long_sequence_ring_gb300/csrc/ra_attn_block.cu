@@ -79,11 +79,11 @@ struct BlockPolicy {
     nkv = block_n_kv(a, qt);
   }
   __device__ int tiles() const { return nkv > 0 ? 1 : 0; }
-  __device__ int hq0() const { return h0; }
   __device__ int kvh() const { return g; }
   __device__ void set_tile(int) {}
-  __device__ int32_t q_row() const { return qt * BM; }
-  __device__ int q_valid() const { return min(BM, p.Tq - qt * BM); }
+  __device__ int q_head(int h) const { return h0 + h; }
+  __device__ int32_t q_row(int) const { return qt * BM; }
+  __device__ int q_valid(int) const { return min(BM, p.Tq - qt * BM); }
   __device__ int n_kv() const { return nkv; }
   __device__ void kv_begin(KvPos& k) const { k.kt = -1; }
   __device__ bool kv_next(KvPos& k) const {
@@ -91,7 +91,7 @@ struct BlockPolicy {
     k.row = k.kt * BN;
     return true;
   }
-  __device__ void mask(const KvPos& k, int row, int& col_lim, bool& masked) const {
+  __device__ void mask(const KvPos& k, int, int row, int& col_lim, bool& masked) const {
     block_mask(p, qt, k.kt, row, col_lim, masked);
   }
   __device__ void store_o(int h, int row, int col0, const uint32_t (&o)[32], float inv_l) const {
@@ -106,7 +106,7 @@ struct BlockPolicy {
     p.lse[static_cast<int64_t>(qt * BM + row) * p.Hq + h0 + h] = lse;
   }
   __device__ void write_empty(int tid, int nthreads) const {
-    const int qv = q_valid();
+    const int qv = q_valid(0);
     for (int i = tid; i < 2 * qv * D; i += nthreads) {
       const int h = i / (qv * D), r = (i / D) % qv, e = i % D;
       const int64_t at = static_cast<int64_t>(qt * BM + r) * p.Hq + h0 + h;

@@ -1,13 +1,16 @@
 // Two-head tcgen05 attention pipeline shared by the ring-order kernel and the
 // block-partial kernel.  A schedule policy Pol supplies (device side):
 //   Pol(const Args&, int item)          decode the CTA's work item
-//   int tiles()                          query tiles of the CTA (1 or 2)
-//   int hq0(), kvh()                     the two query heads hq0, hq0+1 and their K/V head
+//   int tiles()                          query tiles of the CTA, one after the other (0, 1 or 2)
+//   int kvh()                            the K/V head both slots read
 //   void set_tile(int ti)                select query tile ti
-//   int32_t q_row(); int q_valid()       TMA row of its first query, valid rows
+//   int q_head(int h); int32_t q_row(int h); int q_valid(int h)
+//                                        slot h (0, 1) of the tile: its query head, the TMA
+//                                        row of its first query and its valid rows (two heads
+//                                        of a GQA group, or two adjacent query tiles of one head)
 //   int n_kv()                           K/V tiles the query tile meets
 //   KvPos; kv_begin(KvPos&); bool kv_next(KvPos&)   those tiles in order (KvPos::row = TMA row)
-//   void mask(const KvPos&, int row, int& col_lim, bool& masked)
+//   void mask(const KvPos&, int h, int row, int& col_lim, bool& masked)
 //   void store_o(int h, int row, int col0, const uint32_t (&o)[32], float inv_l)
 //   void store_lse(int h, int row, float lse)
 //   void write_empty(int tid, int nthreads)   outputs of a CTA with no query tile to run (tiles() == 0)
@@ -20,21 +23,23 @@ namespace {
 using namespace ra::sm100;
 
 // ===========================================================================
-// Two-head tcgen05 attention kernel, templated on a schedule policy: a CTA runs
-// two query heads that read the same K/V head (a GQA pair), so every K/V tile
-// TMA brings in feeds two score tiles.  The policy supplies the query tiles of
-// the CTA, the K/V tiles each one meets (and in which order), the causal mask
-// and where the output goes: ring order over virtual ranks for the ring kernel,
-// a plain key range at absolute positions for block partials.
+// Two-slot tcgen05 attention kernel, templated on a schedule policy: a CTA
+// runs two 128-row query tiles ("slots") that read the same K/V tiles, so
+// every K/V tile TMA brings in feeds two score tiles.  The slots are two query
+// heads of one GQA group at the same rows, or two adjacent query tiles of one
+// head (which meet the same keys up to one diagonal tile).  The policy
+// supplies the slots, the K/V tiles they meet (and in which order), the causal
+// mask and where the output goes: ring order over virtual ranks for the ring
+// kernel, a plain key range at absolute positions for block partials.
 // Roles (384 threads): warp 0 TMA, warp 1 TMEM allocation + MMA issue, warps
-// 4..7 softmax of head 0, warps 8..11 softmax of head 1 (warps 2, 3 idle).
+// 4..7 softmax of slot 0, warps 8..11 softmax of slot 1 (warps 2, 3 idle).
 // Tensor memory: S_h = cols [128h, 128h+128), O_h = cols [256+128h, ...).
 // P_h (bf16, two per column) overwrites the first 64 columns of S_h and is
 // the A operand of O_h += P_h V straight from tensor memory, so P never
 // touches shared memory.  One thread issues every MMA, in the order
 //   PV0_j, S0_{j+1}, PV1_j, S1_{j+1}
-// which staggers the two heads: each softmax warpgroup works while the tensor
-// core serves the other head (measured faster than one issuer per head).
+// which staggers the two slots: each softmax warpgroup works while the tensor
+// core serves the other slot (measured faster than one issuer per slot).
 // tcgen05 operations of one thread execute in issue order, so S_h(j+1) may
 // overwrite the columns PV_h(j) reads.  A softmax warpgroup only waits for
 // the previous P.V when it must rescale O (lazy rescale, threshold 2^8).
@@ -116,10 +121,11 @@ __global__ void __launch_bounds__(kThreads2, 1)
         if (!(ok = mbar_wait(smem_u32(&sm.q_empty), (ti & 1) ^ 1, abort_flag, lim, 101))) break;
         const uint32_t qb = smem_u32(&sm.q_full);
         mbar_arrive_expect_tx(qb, 2 * kTileBytes);
-        const int32_t qrow = pol.q_row();
-        for (int h = 0; h < 2; ++h)
+        for (int h = 0; h < 2; ++h) {
+          const int32_t qrow = pol.q_row(h);
           for (int s = 0; s < SLABS; ++s)
-            tma_load_3d(smem_u32(sm.q[h] + s * BM * 128), &tmQ, qb, 64 * s, pol.hq0() + h, qrow);
+            tma_load_3d(smem_u32(sm.q[h] + s * BM * 128), &tmQ, qb, 64 * s, pol.q_head(h), qrow);
+        }
         typename Pol::KvPos kp;
         pol.kv_begin(kp);
         while (pol.kv_next(kp)) {
@@ -235,7 +241,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
     bool ok = true;
     for (int ti = 0; ti < n_tiles && ok; ++ti) {
       pol.set_tile(ti);
-      const int q_valid = pol.q_valid();
+      const int q_valid = pol.q_valid(h);
       const int nkv = pol.n_kv();
       typename Pol::KvPos kp;
       pol.kv_begin(kp);
@@ -247,7 +253,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
         tc_fence_after();
         int col_lim;
         bool masked;
-        pol.mask(kp, row, col_lim, masked);
+        pol.mask(kp, h, row, col_lim, masked);
         uint32_t pk[BN / 2];
         const float alpha = softmax_row(t_lane + colS, j, masked, col_lim, args.scale_log2, m, l, pk);
         if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {

@@ -181,7 +181,8 @@ def ring_attn_fwd(q, k, v, causal: bool, n_ranks: int, B: int = 1, scale: Option
     """Ring-order attention forward.  q [B*S, Hq, d], k/v [B*S, Hkv, d] token-major.
 
     Returns (O [B*S, Hq, d] in q's dtype, LSE float32 [B*S, Hq]).  ``variant`` picks the
-    bf16 kernel (0 automatic, 1 one head per CTA, 2 two GQA heads per CTA)."""
+    bf16 kernel (0 automatic, 1 one head per CTA, 2 two GQA heads per CTA, 3 two adjacent query
+    tiles of one head per CTA)."""
     _need_cuda(q, k, v, o, lse)
     rows, Hq, d = q.shape
     Hkv = k.shape[1]

@@ -160,12 +160,15 @@ ra_status ra_ring_attn_fwd(const void* q, const void* k, const void* v, void* o,
                            ra_layout layout, ra_stream stream);
 
 /* Same as ra_ring_attn_fwd with an explicit bf16 kernel variant:
- * 0 = automatic (2 when Hq/Hkv is even, else 1);
+ * 0 = automatic (2 when Hq/Hkv is even, else 3);
  * 1 = one query head per CTA (mirrored pair of query tiles, 128-key tiles,
  *     P via shared memory);
  * 2 = two query heads of one GQA group per CTA sharing every 128-key K/V tile
- *     (needs an even Hq/Hkv; P stays in tensor memory).
- * The variant is ignored for RA_F32.  Both variants agree to rounding. */
+ *     (needs an even Hq/Hkv; P stays in tensor memory);
+ * 3 = two adjacent 128-row query tiles of one head per CTA sharing every K/V
+ *     tile (any Hq/Hkv; same pipeline as 2).  Each call on this variant reads
+ *     the current device's SM count to size its grid.
+ * The variant is ignored for RA_F32.  All variants agree to rounding. */
 ra_status ra_ring_attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse,
                               int32_t B, int32_t Hq, int32_t Hkv, int32_t S, int32_t d,
                               ra_dtype dt, int32_t causal, int32_t n_ranks, float scale,

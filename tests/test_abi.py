@@ -69,6 +69,10 @@ def test_attention_argument_validation(ra):
     assert run(d=96) == ra.RA_ERR_UNSUPPORTED
     assert run(layout=7) == ra.RA_ERR_INVALID_ARG
     assert run(dt=5) == ra.RA_ERR_INVALID_ARG
+    assert _call(ra, "ra_ring_attn_fwd_ex", p, p, p, p, p, 1, 4, 2, 256, 128, 1, 1, 2, 0.0, 0, 4, None) == \
+        ra.RA_ERR_INVALID_ARG and "variant" in ra.last_error()
+    assert _call(ra, "ra_ring_attn_fwd_ex", p, p, p, p, p, 1, 6, 2, 256, 128, 1, 1, 2, 0.0, 0, 2, None) == \
+        ra.RA_ERR_INVALID_ARG and "even" in ra.last_error()
     q = ctypes.c_void_p(24)  # misaligned
     assert _call(ra, "ra_ring_attn_fwd", q, p, p, p, p, 1, 4, 2, 256, 128, 1, 1, 2, 0.0, 0, None) == \
         ra.RA_ERR_INVALID_ARG

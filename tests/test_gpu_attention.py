@@ -69,7 +69,7 @@ def test_fp32_ragged_and_gqa(ra, S, N, causal, Hq, Hkv, d):
     (256, 1, 1, 4, 2, 128, True),      # one virtual rank: the ring is a single step
     (384, 1, 2, 2, 2, 128, False),
 ])
-@pytest.mark.parametrize("variant", [1, 2])
+@pytest.mark.parametrize("variant", [1, 2, 3])
 def test_bf16_parity_small(ra, S, N, B, Hq, Hkv, d, causal, variant):
     if variant == 2 and (Hq // Hkv) % 2:
         Hq = 2 * Hq                       # the two-head kernel needs an even GQA group
@@ -79,7 +79,7 @@ def test_bf16_parity_small(ra, S, N, B, Hq, Hkv, d, causal, variant):
 
 
 @pytest.mark.parametrize("case", ["sharp_scale", "growing_keys"])
-@pytest.mark.parametrize("variant", [1, 2])
+@pytest.mark.parametrize("variant", [1, 2, 3])
 def test_bf16_rescale_paths(ra, case, variant):
     """Inputs that make the running max grow inside and across K/V tiles, so the lazy
     reference fails its check often: the two-pass fallback and the O rescale in tensor
@@ -100,7 +100,7 @@ def test_bf16_rescale_paths(ra, case, variant):
     assert_parity(o, O, lse, L, torch.bfloat16, "%s v%d" % (case, variant))
 
 
-@pytest.mark.parametrize("other", [2])
+@pytest.mark.parametrize("other", [2, 3])
 def test_bf16_variants_agree(ra, other):
     B, S, Hq, Hkv, d, N = 1, 2560, 8, 2, 128, 5
     _, _, _, o1, l1 = _run(ra, 6, B, S, Hq, Hkv, d, N, True, torch.bfloat16, variant=1)
@@ -174,6 +174,22 @@ def test_bf16_gqa_32k_zigzag_with_restore_round_trip(ra):
     c = S // (2 * N)
     for b in range(B):
         _check_sampled(o, lse, seed, b, S, Hq, Hkv, d, _sample_rows(S, N, c, rng, 32))
+
+
+@pytest.mark.parametrize("Hq,Hkv,variant", [(24, 8, 0), (8, 8, 3)])
+def test_bf16_odd_group_32k_adjacent_tiles(ra, Hq, Hkv, variant):
+    """S=32768, N=8 zigzag ranks, GQA group 3 (automatic choice) and plain multi-head attention,
+    on the adjacent-tile schedule with mirrored pairs (enough work to fill the GPU twice over);
+    sampled rows against the oracle."""
+    B, S, d, N, seed = 1, 32768, 128, 8, 8
+    q, k, v = _device_inputs(ra, seed, B, S, Hq, Hkv, d)
+    perm, restore = ra.zigzag_partition([S] * B, N)
+    qz, kz, vz = (ra.gather_rows(x, perm) for x in (q, k, v))
+    oz, lz = ra.ring_attn_fwd(qz, kz, vz, True, N, B=B, layout="zigzag", variant=variant)
+    o, lse = ra.gather_rows(oz, restore), ra.gather_rows(lz, restore)
+    check_status(ra)
+    c = S // (2 * N)
+    _check_sampled(o, lse, seed, 0, S, Hq, Hkv, d, _sample_rows(S, N, c, np.random.default_rng(81), 24))
 
 
 def test_bf16_long_context_131k(ra):
