@@ -19,10 +19,12 @@ using namespace ra::sm100;
 // chunked prefill), causal by absolute position.  Output: the partial's O
 // (fp32, already normalised by its own row sum) and LSE, to be combined with
 // other partials by the LSE merge.  A row with no visible key gets O = 0 and
-// LSE = -inf.  Even GQA groups run the two-head kernel with BlockPolicy; odd
-// groups run the one-head kernel below: one CTA per (128-row query tile, query
-// head), with the pipeline of the one-head ring kernel (TMA producer, one MMA
-// thread, a softmax warpgroup, P via shared memory, double-buffered S).
+// LSE = -inf.  Even GQA groups run the two-slot kernel with BlockPolicy (two
+// heads per CTA); odd groups with at least two query tiles run it with
+// BlockTilePolicy (two adjacent query tiles per CTA); a single query tile of an
+// odd group runs the one-head kernel below: one CTA per (128-row query tile,
+// query head), with the pipeline of the one-head ring kernel (TMA producer,
+// one MMA thread, a softmax warpgroup, P via shared memory, double-buffered S).
 // ===========================================================================
 struct BlockParams {
   int Tq, Tk, Hq, Hkv, group, causal;
@@ -112,6 +114,63 @@ struct BlockPolicy {
       const int64_t at = static_cast<int64_t>(qt * BM + r) * p.Hq + h0 + h;
       p.o[at * D + e] = 0.f;
       if (e == 0) p.lse[at] = -CUDART_INF_F;
+    }
+  }
+};
+
+// Block schedule on adjacent query tiles, for any GQA group: one query head,
+// query tiles 2i and 2i+1 as the two slots, the key tiles the later one meets
+// (under the causal mask a superset of the earlier tile's).  A slot past the
+// last query tile is empty.
+template <int D>
+struct BlockTilePolicy {
+  using Args = BlockParams;
+  using KvPos = typename BlockPolicy<D>::KvPos;
+  const BlockParams& p;
+  int qp, hq, g, ntq, nkv;
+  __device__ BlockTilePolicy(const BlockParams& a, int idx) : p(a) {
+    hq = idx % a.Hq;
+    qp = idx / a.Hq;
+    g = hq / a.group;
+    ntq = (a.Tq + BM - 1) / BM;
+    nkv = block_n_kv(a, min(2 * qp + 1, ntq - 1));
+  }
+  __device__ int tiles() const { return nkv > 0 ? 1 : 0; }
+  __device__ int kvh() const { return g; }
+  __device__ void set_tile(int) {}
+  __device__ int q_head(int) const { return hq; }
+  __device__ int32_t q_row(int h) const { return (2 * qp + h) * BM; }
+  __device__ int q_valid(int h) const { return max(0, min(BM, p.Tq - (2 * qp + h) * BM)); }
+  __device__ int n_kv() const { return nkv; }
+  __device__ void kv_begin(KvPos& k) const { k.kt = -1; }
+  __device__ bool kv_next(KvPos& k) const {
+    if (++k.kt >= nkv) return false;
+    k.row = k.kt * BN;
+    return true;
+  }
+  __device__ void mask(const KvPos& k, int h, int row, int& col_lim, bool& masked) const {
+    block_mask(p, 2 * qp + h, k.kt, row, col_lim, masked);
+  }
+  __device__ void store_o(int h, int row, int col0, const uint32_t (&o)[32], float inv_l) const {
+    float* dst = p.o + (static_cast<int64_t>((2 * qp + h) * BM + row) * p.Hq + hq) * D + col0;
+#pragma unroll
+    for (int i = 0; i < 32; i += 4)
+      *reinterpret_cast<float4*>(dst + i) =
+          make_float4(__uint_as_float(o[i]) * inv_l, __uint_as_float(o[i + 1]) * inv_l,
+                      __uint_as_float(o[i + 2]) * inv_l, __uint_as_float(o[i + 3]) * inv_l);
+  }
+  __device__ void store_lse(int h, int row, float lse) const {
+    p.lse[static_cast<int64_t>((2 * qp + h) * BM + row) * p.Hq + hq] = lse;
+  }
+  __device__ void write_empty(int tid, int nthreads) const {
+    for (int h = 0; h < 2; ++h) {
+      const int qv = q_valid(h);
+      for (int i = tid; i < qv * D; i += nthreads) {
+        const int r = i / D, e = i % D;
+        const int64_t at = static_cast<int64_t>((2 * qp + h) * BM + r) * p.Hq + hq;
+        p.o[at * D + e] = 0.f;
+        if (e == 0) p.lse[at] = -CUDART_INF_F;
+      }
     }
   }
 };
@@ -341,6 +400,16 @@ ra_status launch_block(const void* q, const void* k, const void* v, const BlockP
     const int64_t grid = ra::ceil_div(bp.Tq, BM) * (bp.Hq / 2);
     attn_pair_kernel<D, BlockPolicy<D>><<<static_cast<unsigned>(grid), kThreads2, smem, stream>>>(mq, mk, mv, bp);
     RA_LAUNCH_CHECK("attn_pair_kernel<BlockPolicy>");
+    return RA_OK;
+  }
+  if (ra::ceil_div(bp.Tq, BM) >= 2) {  // two adjacent query tiles of one head per CTA
+    const size_t smem = sizeof(Smem2<D>) + 1024;
+    RA_CUDA_TRY(cudaFuncSetAttribute(attn_pair_kernel<D, BlockTilePolicy<D>>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)));
+    const int64_t grid = ra::ceil_div(ra::ceil_div(bp.Tq, BM), 2) * bp.Hq;
+    attn_pair_kernel<D, BlockTilePolicy<D>><<<static_cast<unsigned>(grid), kThreads2, smem, stream>>>(mq, mk, mv,
+                                                                                                       bp);
+    RA_LAUNCH_CHECK("attn_pair_kernel<BlockTilePolicy>");
     return RA_OK;
   }
   const size_t smem = sizeof(Smem<D>) + 1024;

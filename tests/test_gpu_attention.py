@@ -212,6 +212,9 @@ def test_bf16_long_context_131k(ra):
     (77, 1000, 5000, 0, True, 8, 2, 64),      # every key visible
     (200, 333, 0, 0, False, 4, 1, 128),       # non-causal
     (256, 128, 0, 300, True, 2, 1, 128),      # no key visible to any row of the block
+    (300, 500, 400, 0, True, 3, 1, 128),      # odd group, adjacent query tiles, last pair half empty
+    (640, 300, 0, 200, True, 5, 5, 64),       # multi-head: early tile pairs see no key, later ones some
+    (384, 256, 0, 0, False, 3, 3, 128),       # multi-head, non-causal
 ])
 def test_block_partial_matches_oracle(ra, Tq, Tk, q0, k0, causal, Hq, Hkv, d):
     q = I.synth_normal(71, I.TID_Q, (Tq, Hq, d), torch.bfloat16)
@@ -228,7 +231,8 @@ def test_block_partial_matches_oracle(ra, Tq, Tk, q0, k0, causal, Hq, Hkv, d):
     assert np.abs(lg[live] - L[live]).max(initial=0) <= 1e-3
 
 
-@pytest.mark.parametrize("ctx,Tq,seg,Hq,Hkv", [(3000, 700, 1024, 4, 2), (513, 255, 128, 2, 1), (0, 600, 200, 4, 4)])
+@pytest.mark.parametrize("ctx,Tq,seg,Hq,Hkv", [(3000, 700, 1024, 4, 2), (513, 255, 128, 2, 1), (0, 600, 200, 4, 4),
+                                               (3000, 700, 1024, 3, 1)])
 def test_segmented_prefill_matches_full_attention(ra, ctx, Tq, seg, Hq, Hkv):
     """A chunk of Tq new tokens after ctx cached ones attends causally to all ctx+Tq keys, in
     segments of seg keys merged by LSE; equal to the plain attention rows."""
