@@ -270,12 +270,54 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
 // One warp per (token, head) row: LSE = M + ln sum_p e^{LSE_p - M},
 // O = sum_p e^{LSE_p - LSE} O_p (partials with LSE_p = -inf skipped).
 template <bool OUT_BF16>
+__device__ __forceinline__ void store_merged(void* o_out, int64_t at, const float4& a) {
+  if (OUT_BF16) {
+    uint2 pk = make_uint2(pack_bf16(a.x, a.y), pack_bf16(a.z, a.w));
+    *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(o_out) + at) = pk;
+  } else {
+    *reinterpret_cast<float4*>(static_cast<float*>(o_out) + at) = a;
+  }
+}
+
+template <bool OUT_BF16>
 __global__ void lse_merge_kernel(const float* __restrict__ o_parts, const float* __restrict__ lse_parts,
                                  int P, int64_t rows, int d, void* __restrict__ o_out,
                                  float* __restrict__ lse_out) {
   const int lane = threadIdx.x & 31;
   const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  if (P <= 8 && d == 128) {
+    // Few partials (segmented prefill, stand-alone merges): lane p holds partial p's
+    // LSE and weight, and the warp's loads of all P partial rows are issued together,
+    // independent of the LSE arithmetic, so a row costs one memory latency.
+    for (int64_t row = warp; row < rows; row += nwarps) {
+      float4 v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (u < P) v[u] = *reinterpret_cast<const float4*>(o_parts + (static_cast<int64_t>(u) * rows + row) * 128 + 4 * lane);
+      const float x = lane < P ? lse_parts[static_cast<int64_t>(lane) * rows + row] : -CUDART_INF_F;
+      float M = x;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+      const float wu = (x == -CUDART_INF_F) ? 0.f : expf(x - M);
+      float tot = wu;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+      const float w = tot > 0.f ? wu / tot : 0.f;   // e^{LSE_p - LSE}
+      float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (u >= P) break;
+        const float wp = __shfl_sync(0xffffffffu, w, u);
+        if (wp != 0.f) {   // an empty partial's O is never read
+          a.x += wp * v[u].x; a.y += wp * v[u].y; a.z += wp * v[u].z; a.w += wp * v[u].w;
+        }
+      }
+      store_merged<OUT_BF16>(o_out, row * 128 + 4 * lane, a);
+      if (lse_out && lane == 0) lse_out[row] = (M == -CUDART_INF_F) ? -CUDART_INF_F : M + logf(tot);
+    }
+    return;
+  }
   for (int64_t row = warp; row < rows; row += nwarps) {
     float M = -CUDART_INF_F;
     for (int pp = lane; pp < P; pp += 32) M = fmaxf(M, lse_parts[static_cast<int64_t>(pp) * rows + row]);
@@ -301,12 +343,7 @@ __global__ void lse_merge_kernel(const float* __restrict__ o_parts, const float*
           a.x += wgt * v.x; a.y += wgt * v.y; a.z += wgt * v.z; a.w += wgt * v.w;
         }
       }
-      if (OUT_BF16) {
-        uint2 pk = make_uint2(pack_bf16(a.x, a.y), pack_bf16(a.z, a.w));
-        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(o_out) + row * d + e0) = pk;
-      } else {
-        *reinterpret_cast<float4*>(static_cast<float*>(o_out) + row * d + e0) = a;
-      }
+      store_merged<OUT_BF16>(o_out, row * d + e0, a);
     }
     if (lse_out && lane == 0) lse_out[row] = lse;
   }

@@ -68,7 +68,8 @@ def test_gather_out_of_range_index_is_reported(ra):
 
 # --------------------------------------------------------------------- merge
 
-@pytest.mark.parametrize("P,T,H,d", [(1, 5, 3, 8), (3, 17, 4, 128), (64, 64, 32, 128), (8, 2, 2, 64)])
+@pytest.mark.parametrize("P,T,H,d", [(1, 5, 3, 8), (3, 17, 4, 128), (64, 64, 32, 128), (8, 2, 2, 64),
+                                     (8, 300, 8, 128), (9, 40, 4, 128), (1, 33, 2, 128)])
 @pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
 def test_lse_merge(ra, P, T, H, d, out_dtype):
     g = torch.Generator().manual_seed(P * 1000 + T)
