@@ -279,8 +279,8 @@ __device__ __forceinline__ void store_merged(void* o_out, int64_t at, const floa
   }
 }
 
-// MODE 1: at most 8 partials, d = 128; MODE 2: at most 256 partials, d = 128;
-// MODE 0: any P and d.  Separate instances keep each path's register count.
+// MODE 1: at most 8 partials, d = 128; MODE 0: any P and d.  Separate
+// instances keep the fast path's register count (and so its occupancy).
 template <bool OUT_BF16, int MODE>
 __global__ void lse_merge_kernel(const float* __restrict__ o_parts, const float* __restrict__ lse_parts,
                                  int P, int64_t rows, int d, void* __restrict__ o_out,
@@ -314,57 +314,6 @@ __global__ void lse_merge_kernel(const float* __restrict__ o_parts, const float*
         if (wp != 0.f) {   // an empty partial's O is never read
           a.x += wp * v[u].x; a.y += wp * v[u].y; a.z += wp * v[u].z; a.w += wp * v[u].w;
         }
-      }
-      store_merged<OUT_BF16>(o_out, row * 128 + 4 * lane, a);
-      if (lse_out && lane == 0) lse_out[row] = (M == -CUDART_INF_F) ? -CUDART_INF_F : M + logf(tot);
-    }
-    return;
-  }
-  if (MODE == 2) {
-    // Many partials, most of them empty (the decode's splits past a request's
-    // context): lane l holds the LSEs and weights of partials l, l+32, ...; the
-    // O rows of the non-empty ones are then read 16 at a time, all 16 loads in
-    // flight together.
-    for (int64_t row = warp; row < rows; row += nwarps) {
-      float x[8], w[8];
-      float M = -CUDART_INF_F;
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const int pp = q * 32 + lane;
-        x[q] = pp < P ? lse_parts[static_cast<int64_t>(pp) * rows + row] : -CUDART_INF_F;
-        M = fmaxf(M, x[q]);
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-      float tot = 0.f;
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        w[q] = (x[q] == -CUDART_INF_F) ? 0.f : expf(x[q] - M);
-        tot += w[q];
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
-      const float inv = tot > 0.f ? 1.f / tot : 0.f;
-      float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int p0 = 0; p0 < P; p0 += 16) {
-        float4 v[16];
-        float wp[16];
-#pragma unroll
-        for (int u = 0; u < 16; ++u) {
-          const int pp = p0 + u;   // warp-uniform
-          float wq = 0.f;
-#pragma unroll
-          for (int q = 0; q < 8; ++q)
-            if ((pp >> 5) == q) wq = __shfl_sync(0xffffffffu, w[q], pp & 31);
-          wp[u] = pp < P ? wq * inv : 0.f;
-          if (wp[u] != 0.f)   // an empty partial's O is never read
-            v[u] = *reinterpret_cast<const float4*>(o_parts + (static_cast<int64_t>(pp) * rows + row) * 128 + 4 * lane);
-        }
-#pragma unroll
-        for (int u = 0; u < 16; ++u)
-          if (wp[u] != 0.f) {
-            a.x += wp[u] * v[u].x; a.y += wp[u] * v[u].y; a.z += wp[u] * v[u].z; a.w += wp[u] * v[u].w;
-          }
       }
       store_merged<OUT_BF16>(o_out, row * 128 + 4 * lane, a);
       if (lse_out && lane == 0) lse_out[row] = (M == -CUDART_INF_F) ? -CUDART_INF_F : M + logf(tot);
@@ -405,11 +354,10 @@ __global__ void lse_merge_kernel(const float* __restrict__ o_parts, const float*
 ra_status launch_merge(const float* o_parts, const float* lse_parts, int P, int64_t rows, int d,
                        void* o_out, ra_dtype out_dt, float* lse_out, cudaStream_t stream) {
   const int64_t blocks = std::min<int64_t>(ra::ceil_div(rows * 32, 256), 152 * 16);
-  const int mode = d != 128 ? 0 : (P <= 8 ? 1 : (P <= 256 ? 2 : 0));
+  const int mode = (d == 128 && P <= 8) ? 1 : 0;
   const bool bf = out_dt == RA_BF16;
 #define RA_MERGE(B, M) lse_merge_kernel<B, M><<<blocks, 256, 0, stream>>>(o_parts, lse_parts, P, rows, d, o_out, lse_out)
   if (mode == 1) { if (bf) RA_MERGE(true, 1); else RA_MERGE(false, 1); }
-  else if (mode == 2) { if (bf) RA_MERGE(true, 2); else RA_MERGE(false, 2); }
   else { if (bf) RA_MERGE(true, 0); else RA_MERGE(false, 0); }
 #undef RA_MERGE
   RA_LAUNCH_CHECK("lse_merge_kernel");
