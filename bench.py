@@ -211,7 +211,7 @@ class Workload:
     def _prefill(self, e):
         ra, P = self.ra, PREFILL
         # a1: head-tail partition of the batch (device kernel), a2: gather to rank-major layout
-        ra.lib().ra_zigzag_partition((ra._c.c_int64 * 1)(P["S"]), 1, P["N"], self.perm.data_ptr(),
+        ra.lib().ra_zigzag_partition((ra._c.c_int64 * P["B"])(*([P["S"]] * P["B"])), P["B"], P["N"], self.perm.data_ptr(),
                                      self.restore.data_ptr(), None, None, ra._stream())
         ra.gather_rows(self.q, self.perm, self.qz)
         ra.gather_rows(self.k, self.perm, self.kz)
@@ -606,7 +606,14 @@ def main():
                          "'rope' (the RoPE prologue, needs 'prefill') to run only those parts (profiler captures)")
     ap.add_argument("--prefill-seq", type=int, default=None, help="override S of the prefill (multiple of 2N)")
     ap.add_argument("--decode-requests", type=int, default=None, help="override the number of decode requests")
+    ap.add_argument("--prefill-shape", default=None,
+                    help="B,Hq,Hkv,S,N of the prefill, for the parts runs (e.g. 1,8,8,8192,8 or 2,32,8,32768,8)")
     args = ap.parse_args()
+    if args.prefill_shape:
+        if args.parts == "all":
+            ap.error("--prefill-shape is for --parts runs; the benchmark line keeps its workload")
+        B, Hq, Hkv, S, N = (int(x) for x in args.prefill_shape.split(","))
+        PREFILL.update(B=B, Hq=Hq, Hkv=Hkv, S=S, N=N)
     if args.prefill_seq:
         PREFILL["S"] = args.prefill_seq
     if args.decode_requests:
