@@ -192,6 +192,20 @@ def test_bf16_odd_group_32k_adjacent_tiles(ra, Hq, Hkv, variant):
     _check_sampled(o, lse, seed, 0, S, Hq, Hkv, d, _sample_rows(S, N, c, np.random.default_rng(81), 24))
 
 
+@pytest.mark.parametrize("S,N,Hq,Hkv", [(3200, 8, 40, 8), (4800, 8, 40, 8), (4800, 8, 40, 40)])
+def test_bf16_adjacent_tiles_mirrored_ragged(ra, S, N, Hq, Hkv):
+    """Adjacent-tile schedule with mirrored pairs (enough CTAs for two waves) on ragged
+    chunks: 200 rows (two tiles, the second short) and 300 rows (three tiles, so the last
+    pair has an empty slot); sampled rows against the oracle."""
+    B, d, seed = 1, 128, 9
+    q, k, v = _device_inputs(ra, seed, B, S, Hq, Hkv, d)
+    o, lse = ra.ring_attn_fwd(q, k, v, True, N, B=B, variant=3)
+    check_status(ra)
+    c = S // (2 * N)
+    rows = _sample_rows(S, N, c, np.random.default_rng(91), 24)
+    _check_sampled(o, lse, seed, 0, S, Hq, Hkv, d, rows)
+
+
 def test_bf16_long_context_131k(ra):
     """B=1, Hq=32, Hkv=8, S=131072, d=128, causal, N=16 (32 chunks of 4096); sampled rows."""
     B, S, Hq, Hkv, d, N, seed = 1, 131072, 32, 8, 128, 16, 5
