@@ -367,6 +367,12 @@ def run_parts(args, dev):
         out["decode_merge_gbs"] = wl.decode_bytes()[0] / (out["decode_merge_ms"] * 1e-3) / 1e9
     if "rope" in parts:
         out["rope"] = measure_rope(ra, wl)
+    if "reorg" in parts:
+        out["reorg"] = measure_kv_reorg(ra, wl, n_req=min(8, DECODE["R"]))
+    if "merge" in parts:
+        out["merge"] = measure_merge(ra, dev)
+    if "segmented" in parts:
+        out["segmented"] = measure_segmented(ra, dev)
     print(json.dumps(out), flush=True)
 
 
@@ -602,10 +608,12 @@ def main():
     ap.add_argument("--cpu-rows", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--parts", default="all",
-                    help="'all' for the benchmark line, else a comma list of 'prefill', 'decode' and "
-                         "'rope' (the RoPE prologue, needs 'prefill') to run only those parts (profiler captures)")
+                    help="'all' for the benchmark line, else a comma list of 'prefill', 'decode', 'rope' (the "
+                         "RoPE prologue, needs 'prefill'), 'reorg' (the KV reorg, needs 'decode'), 'merge' and "
+                         "'segmented' to run only those parts (profiler captures)")
     ap.add_argument("--prefill-seq", type=int, default=None, help="override S of the prefill (multiple of 2N)")
     ap.add_argument("--decode-requests", type=int, default=None, help="override the number of decode requests")
+    ap.add_argument("--merge-tokens", type=int, default=None, help="override T of the stand-alone merge")
     ap.add_argument("--prefill-shape", default=None,
                     help="B,Hq,Hkv,S,N of the prefill, for the parts runs (e.g. 1,8,8,8192,8 or 2,32,8,32768,8)")
     args = ap.parse_args()
@@ -618,6 +626,8 @@ def main():
         PREFILL["S"] = args.prefill_seq
     if args.decode_requests:
         DECODE["R"] = args.decode_requests
+    if args.merge_tokens:
+        MERGE["T"] = args.merge_tokens
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if args.impl == "reference":
