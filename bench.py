@@ -63,10 +63,13 @@ def _source_hash(names):
     return h.hexdigest()[:16]
 
 
+TRAFFIC_JSON = os.path.join(ROOT, "profiles", "traffic.json")
+
+
 def _traffic(kernel):
     """DRAM bytes per launch from the committed ncu summary, if it is for this source."""
     try:
-        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+        with open(TRAFFIC_JSON) as f:
             t = json.load(f)[kernel]
         if t.get("source_sha256_16") != _source_hash(KERNEL_SOURCES[kernel]):
             return None
