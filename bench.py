@@ -619,7 +619,8 @@ def cpu_baseline(rows):
         dt += t
     return {"value": round(fl / dt / 1e12, 6), "unit": "TFLOP/s", "cores": _threads(), "kind": "oracle",
             "sample": "%d random query rows x 32 heads of the S=131072 causal prefill per call, float64 numpy, "
-                      "%.1f s of CPU time" % (rows, dt)}
+                      "%.1f s of CPU time; the rate is extrapolated to the full prefill (about %.0f s)"
+                      % (rows, dt, causal_flops(PREFILL["B"], PREFILL["Hq"], PREFILL["S"], PREFILL["d"]) / (fl / dt))}
 
 
 WORKLOAD = ("causal GQA ring prefill B=1 Hq=32 Hkv=8 S=131072 d=128 N=16 zigzag ranks "
