@@ -35,7 +35,7 @@ from context_long_sequence_ring_gb300 import inputs as I  # noqa: E402
 
 METRIC = "ring-attn fwd TFLOP/s (causal-adj) & % bf16 peak; decode+merge GB/s % HBM"
 PREFILL = dict(B=1, Hq=32, Hkv=8, S=131072, d=128, N=16, seed=5)
-DECODE = dict(R=64, lo=4096, hi=131072, Hq=32, Hkv=8, d=128, bs=128, I=16, pcp=2, dcp=4, seed=4, split=8)
+DECODE = dict(R=64, lo=4096, hi=131072, Hq=32, Hkv=8, d=128, bs=128, I=16, pcp=2, dcp=4, seed=4, split=16)
 # sources whose contents the recorded DRAM traffic of each kernel was measured on
 KERNEL_SOURCES = {"ring_attn_bf16": ["ra_attn_bf16.cu", "ra_attn_pair.cuh", "ra_attn_tc.cuh", "ra_sm100.cuh"],
                   "cp_decode": ["ra_decode.cu"]}
@@ -680,6 +680,7 @@ def main():
     ap.add_argument("--prefill-seq", type=int, default=None, help="override S of the prefill (multiple of 2N)")
     ap.add_argument("--decode-requests", type=int, default=None, help="override the number of decode requests")
     ap.add_argument("--merge-tokens", type=int, default=None, help="override T of the stand-alone merge")
+    ap.add_argument("--decode-split", type=int, default=None, help="override the decode's virtual blocks per split")
     ap.add_argument("--prefill-shape", default=None,
                     help="B,Hq,Hkv,S,N of the prefill, for the parts runs (e.g. 1,8,8,8192,8 or 2,32,8,32768,8)")
     args = ap.parse_args()
@@ -694,6 +695,8 @@ def main():
         DECODE["R"] = args.decode_requests
     if args.merge_tokens:
         MERGE["T"] = args.merge_tokens
+    if args.decode_split:
+        DECODE["split"] = args.decode_split
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if args.impl == "reference":

@@ -191,9 +191,11 @@ def test_scatter_places_rows_bit_exact(ra):
         assert torch.equal(got, kt[ts])
 
 
-def test_decode_full_size_sampled_requests(ra):
+@pytest.mark.parametrize("split", [16, 8])
+def test_decode_full_size_sampled_requests(ra, split):
     """64 requests, context U[4096, 131072], Hq=32, Hkv=8, d=128, block 128, interleave 16, pcp=2, dcp=4:
-    full-size slot mapping (bit-exact) + scatter + split-KV decode + merge; sampled requests vs the oracle."""
+    full-size slot mapping (bit-exact) + scatter + split-KV decode + merge; sampled requests vs the oracle.
+    Split 16 is the bench's launch configuration."""
     seed, R, bs, I_, pcp, dcp, Hq, Hkv, d = 4, 64, 128, 16, 2, 4, 32, 8, 128
     W = pcp * dcp
     wl = I.decode_workload(seed, R, 4096, 131072, bs, pcp, dcp)
@@ -215,7 +217,7 @@ def test_decode_full_size_sampled_requests(ra):
     vc = torch.empty_like(kc)
     ra.cp_kv_scatter(kt, vt, slot, kc, vc)
     del kt, vt
-    o, lse = ra.cp_decode(qd.to(DEV), kc, vc, wl["block_table"].to(DEV), ctx.to(DEV), I_, pcp, dcp, split_blocks=8)
+    o, lse = ra.cp_decode(qd.to(DEV), kc, vc, wl["block_table"].to(DEV), ctx.to(DEV), I_, pcp, dcp, split_blocks=split)
     check_status(ra)
     Ls = ctx.numpy()
     for r in sorted({int(np.argmin(Ls)), int(np.argmax(Ls)), 17}):
