@@ -403,6 +403,7 @@ def run_ours(args, rank, world, dev):
     line["next_kv_reorg"] = measure_kv_reorg(ra, wl)
     line["next_rope_prologue"] = measure_rope(ra, wl)
     line["merge_stress"] = measure_merge(ra, dev)
+    line["varlen_prefill"] = measure_varlen(ra, dev)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_rows)
     return line
@@ -438,6 +439,8 @@ def run_parts(args, dev):
         out["merge"] = measure_merge(ra, dev)
     if "segmented" in parts:
         out["segmented"] = measure_segmented(ra, dev)
+    if "varlen" in parts:
+        out["varlen"] = measure_varlen(ra, dev)
     print(json.dumps(out), flush=True)
 
 
@@ -500,6 +503,37 @@ def measure_kv_reorg(ra, wl, n_req=8, reps=5):
     gbs = nbytes / (ms * 1e-3) / 1e9
     return {"requests": n_req, "tokens": T, "ms": round(ms, 3), "gbs": round(gbs, 1),
             "frac_of_hbm": round(gbs / _peaks()["hbm"], 4)}
+
+
+VARLEN = dict(lens=[65536, 32768, 16384, 12288, 4096, 100], N=16, Hq=32, Hkv=8, d=128, seed=10)
+
+
+def measure_varlen(ra, dev, reps=5):
+    """Several requests of different lengths in one ring call, on the head-tail gathered layout
+    (the pages' multi-request PCP prefill); causal attention FLOPs of the real tokens only."""
+    V = VARLEN
+    tab = I.normal_table(torch.bfloat16)
+    G = sum(-(-L // (2 * V["N"])) * 2 * V["N"] for L in V["lens"])
+    q = ra.synth_fill(I.tensor_key(V["seed"], I.TID_Q), tab, (G, V["Hq"], V["d"]), dev)
+    k = ra.synth_fill(I.tensor_key(V["seed"], I.TID_K), tab, (G, V["Hkv"], V["d"]), dev)
+    v = ra.synth_fill(I.tensor_key(V["seed"], I.TID_V), tab, (G, V["Hkv"], V["d"]), dev)
+    o, lse = torch.empty_like(q), torch.empty((G, V["Hq"]), dtype=torch.float32, device=dev)
+    for _ in range(2):
+        ra.ring_attn_fwd_varlen(q, k, v, V["lens"], True, V["N"], o=o, lse=lse)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        ra.ring_attn_fwd_varlen(q, k, v, V["lens"], True, V["N"], o=o, lse=lse)
+    e1.record()
+    torch.cuda.synchronize()
+    if ra.device_status() != 0:
+        raise RuntimeError("device status after the varlen prefill: %s" % ra.last_error())
+    ms = e0.elapsed_time(e1) / reps
+    flops = sum(causal_flops(1, V["Hq"], L, V["d"]) for L in V["lens"])
+    tf = flops / (ms * 1e-3) / 1e12
+    return {"config": V, "ms": round(ms, 3), "tflops": round(tf, 1),
+            "frac_of_bf16_sustained": round(tf / _peaks()["bf16_sus"], 4)}
 
 
 MERGE = dict(P=8, T=32768, H=32, d=128, seed=7)
@@ -675,8 +709,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--parts", default="all",
                     help="'all' for the benchmark line, else a comma list of 'prefill', 'decode', 'rope' (the "
-                         "RoPE prologue, needs 'prefill'), 'reorg' (the KV reorg, needs 'decode'), 'merge' and "
-                         "'segmented' to run only those parts (profiler captures)")
+                         "RoPE prologue, needs 'prefill'), 'reorg' (the KV reorg, needs 'decode'), 'merge', "
+                         "'segmented' and 'varlen' to run only those parts (profiler captures)")
     ap.add_argument("--prefill-seq", type=int, default=None, help="override S of the prefill (multiple of 2N)")
     ap.add_argument("--decode-requests", type=int, default=None, help="override the number of decode requests")
     ap.add_argument("--merge-tokens", type=int, default=None, help="override T of the stand-alone merge")

@@ -532,6 +532,111 @@ struct RingTilePolicy {
   __device__ void write_empty(int, int) const {}  // every ring query tile meets at least one key tile
 };
 
+// ------------------------------------------------------------------ varlen
+// Several requests of different lengths in one call, in the layout the
+// head-tail partition gathers them to: rank-major, then request, then the
+// request's chunk r and chunk 2N-1-r.  Request b is padded to L'_b, a
+// multiple of 2N, and cut into chunks of c_b = L'_b / 2N tokens, so its row
+// (rank r, half, offset) is r * T_rank + 2 * pre_b + half * c_b + offset with
+// T_rank = 2 * sum_b c_b and pre_b = sum_{b' < b} c_b'.  Keys at positions at
+// or past the request's real length (the padding) are masked.
+constexpr int kMaxVarlenSeqs = 256;
+
+struct VarlenParams {
+  int num_seqs, Hq, Hkv, group, N, causal, mirrored;
+  int T_rank;
+  float scale_log2;
+  __nv_bfloat16* o;
+  float* lse;
+  long long wait_limit;
+  int items_pre[kMaxVarlenSeqs + 1];  // CTAs before request b
+  int c[kMaxVarlenSeqs];              // chunk length of request b
+  int len[kMaxVarlenSeqs];            // real length of request b
+  int pre[kMaxVarlenSeqs];            // sum of the chunk lengths of requests before b
+};
+
+// Adjacent-tile schedule (as RingTilePolicy) within one request of a varlen call.
+template <int D>
+struct RingVarlenPolicy {
+  using Args = VarlenParams;
+  using KvPos = typename RingPolicy<D>::KvPos;
+  const VarlenParams& p;
+  Sched sch;
+  int b, hq, g, r, jp, qc, pr, ntp;
+  __device__ RingVarlenPolicy(const VarlenParams& a, int idx) : p(a) {
+    int lo = 0, hi = a.num_seqs;   // the request: last b with items_pre[b] <= idx
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (a.items_pre[mid] <= idx) lo = mid; else hi = mid;
+    }
+    b = lo;
+    idx -= a.items_pre[b];
+    const int c = a.c[b], nt = (c + BM - 1) / BM;
+    ntp = (nt + 1) / 2;
+    sch = Sched{a.N, c, nt, a.causal, BN, nt};
+    const int hg = idx % a.group; idx /= a.group;
+    if (a.mirrored) {
+      jp = idx % ntp; idx /= ntp;
+      r = idx % a.N; idx /= a.N;
+      g = idx;
+    } else {
+      g = idx % a.Hkv; idx /= a.Hkv;
+      jp = ntp - 1 - idx % ntp; idx /= ntp;
+      r = 2 * a.N - 1 - idx;
+    }
+    hq = g * a.group + hg;
+    qc = r;
+    pr = jp;
+  }
+  __device__ int32_t row_of(int ch, int off) const {
+    const int rank = ch < p.N ? ch : 2 * p.N - 1 - ch;
+    const int half = ch < p.N ? 0 : 1;
+    return rank * p.T_rank + 2 * p.pre[b] + half * p.c[b] + off;
+  }
+  __device__ int tiles() const { return p.mirrored ? 2 : 1; }
+  __device__ int kvh() const { return g; }
+  __device__ void set_tile(int ti) {
+    if (ti == 0) { qc = r; pr = jp; }
+    else { qc = 2 * p.N - 1 - r; pr = ntp - 1 - jp; }
+  }
+  __device__ int q_head(int) const { return hq; }
+  __device__ int32_t q_row(int h) const { return row_of(qc, (2 * pr + h) * BM); }
+  __device__ int q_valid(int h) const { return max(0, min(BM, p.c[b] - (2 * pr + h) * BM)); }
+  __device__ int kv_tile() const { return min(2 * pr + 1, sch.nt - 1); }
+  __device__ int n_kv() const { return n_kv_tiles(sch, qc, kv_tile()); }
+  __device__ void kv_begin(KvPos& k) const { k.it.init(sch, qc, kv_tile()); }
+  __device__ bool kv_next(KvPos& k) const {
+    if (!k.it.next(k.kc, k.kt)) return false;
+    k.row = row_of(k.kc, k.kt * BN);
+    return true;
+  }
+  __device__ void mask(const KvPos& k, int h, int row, int& col_lim, bool& masked) const {
+    tile_mask(sch, qc, 2 * pr + h, k.kc, k.kt, row, col_lim, masked);
+    const int real = p.len[b] - (k.kc * p.c[b] + k.kt * BN);   // keys of the tile before the padding
+    if (real < col_lim) {
+      col_lim = real > 0 ? real : 0;
+      masked = true;
+    }
+  }
+  __device__ void store_o(int h, int row, int col0, const uint32_t (&o)[32], float inv_l) const {
+    const int64_t trow = row_of(qc, (2 * pr + h) * BM + row);
+    __nv_bfloat16* dst = p.o + (trow * p.Hq + hq) * D + col0;
+#pragma unroll
+    for (int i = 0; i < 32; i += 8) {
+      uint4 pk;
+      pk.x = f2_bf16x2(__uint_as_float(o[i]) * inv_l, __uint_as_float(o[i + 1]) * inv_l);
+      pk.y = f2_bf16x2(__uint_as_float(o[i + 2]) * inv_l, __uint_as_float(o[i + 3]) * inv_l);
+      pk.z = f2_bf16x2(__uint_as_float(o[i + 4]) * inv_l, __uint_as_float(o[i + 5]) * inv_l);
+      pk.w = f2_bf16x2(__uint_as_float(o[i + 6]) * inv_l, __uint_as_float(o[i + 7]) * inv_l);
+      *reinterpret_cast<uint4*>(dst + i) = pk;
+    }
+  }
+  __device__ void store_lse(int h, int row, float lse) const {
+    p.lse[static_cast<int64_t>(row_of(qc, (2 * pr + h) * BM + row)) * p.Hq + hq] = lse;
+  }
+  __device__ void write_empty(int, int) const {}  // every query tile meets at least its own first key tile
+};
+
 // Per-rank tile classification with the kernels' own iterator (for tests):
 // visited tiles that need no mask, visited tiles with a causal mask, skipped.
 __global__ void schedule_counts_kernel(Sched s, unsigned long long* counts) {
@@ -593,6 +698,23 @@ ra_status launch_bf16(const void* q, const void* k, const void* v, const Params&
   return RA_OK;
 }
 
+template <int D>
+ra_status launch_varlen(const void* q, const void* k, const void* v, int64_t rows, const VarlenParams& prm,
+                        int64_t items, cudaStream_t stream) {
+  CUtensorMap mq, mk, mv;
+  ra_status st;
+  if ((st = make_map(&mq, q, D, prm.Hq, rows)) != RA_OK) return st;
+  if ((st = make_map(&mk, k, D, prm.Hkv, rows)) != RA_OK) return st;
+  if ((st = make_map(&mv, v, D, prm.Hkv, rows)) != RA_OK) return st;
+  const size_t smem = sizeof(Smem2<D>) + 1024;
+  RA_CUDA_TRY(cudaFuncSetAttribute(attn_pair_kernel<D, RingVarlenPolicy<D>>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)));
+  attn_pair_kernel<D, RingVarlenPolicy<D>><<<static_cast<unsigned>(items), kThreads2, smem, stream>>>(mq, mk, mv,
+                                                                                                       prm);
+  RA_LAUNCH_CHECK("attn_pair_kernel<RingVarlenPolicy>");
+  return RA_OK;
+}
+
 }  // namespace
 
 namespace ra {
@@ -647,6 +769,63 @@ extern "C" ra_status ra_ring_attn_fwd_ex(const void* q, const void* k, const voi
   }
   if (d == 128) return launch_bf16<128>(q, k, v, prm, variant, stream);
   return launch_bf16<64>(q, k, v, prm, variant, stream);
+}
+
+extern "C" ra_status ra_ring_attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                                             const int64_t* seq_lens, int32_t num_seqs, int32_t Hq, int32_t Hkv,
+                                             int32_t d, ra_dtype dt, int32_t causal, int32_t n_ranks, float scale,
+                                             ra_stream stream) {
+  ra::clear_error();
+  RA_REQUIRE(seq_lens != nullptr, "seq_lens is NULL");
+  RA_REQUIRE(num_seqs >= 1 && num_seqs <= kMaxVarlenSeqs, "num_seqs must be in [1, %d] (got %d)", kMaxVarlenSeqs,
+             num_seqs);
+  RA_REQUIRE(Hq >= 1 && Hkv >= 1, "Hq, Hkv must be >= 1");
+  RA_REQUIRE(Hq % Hkv == 0, "Hq (%d) must be a multiple of Hkv (%d)", Hq, Hkv);
+  RA_REQUIRE(n_ranks >= 1, "n_ranks must be >= 1 (got %d)", n_ranks);
+  RA_REQUIRE(dt == RA_F32 || dt == RA_BF16, "unknown dtype");
+  if (dt != RA_BF16) return ra::fail(RA_ERR_UNSUPPORTED, "the varlen call runs on bf16 inputs only");
+  if (d != 64 && d != 128) return ra::fail(RA_ERR_UNSUPPORTED, "head dim %d not supported (64 or 128)", d);
+  VarlenParams prm;
+  prm.num_seqs = num_seqs; prm.Hq = Hq; prm.Hkv = Hkv; prm.group = Hq / Hkv; prm.N = n_ranks;
+  prm.causal = causal ? 1 : 0;
+  int64_t G = 0, csum = 0, pairs = 0;
+  for (int b = 0; b < num_seqs; ++b) {
+    RA_REQUIRE(seq_lens[b] >= 0, "negative sequence length at %d", b);
+    const int64_t Lp = ra::ceil_div(seq_lens[b], 2 * n_ranks) * 2 * n_ranks;
+    RA_REQUIRE(Lp < (int64_t(1) << 31), "sequence %d too long", b);
+    prm.c[b] = static_cast<int>(Lp / (2 * n_ranks));
+    prm.len[b] = static_cast<int>(seq_lens[b]);
+    prm.pre[b] = static_cast<int>(csum);
+    csum += prm.c[b];
+    G += Lp;
+    pairs += (ra::ceil_div(prm.c[b], BM) + 1) / 2;
+    RA_REQUIRE(G < (int64_t(1) << 31), "total padded length must be < 2^31");
+  }
+  if (G == 0) return RA_OK;
+  RA_REQUIRE(q && k && v && o && lse, "NULL pointer");
+  RA_REQUIRE(ra::aligned16(q) && ra::aligned16(k) && ra::aligned16(v) && ra::aligned16(o) &&
+                 reinterpret_cast<uintptr_t>(lse) % 4 == 0,
+             "q, k, v, o must be 16-byte aligned");
+  prm.T_rank = static_cast<int>(2 * csum);
+  int dev = 0, sms = 0;
+  RA_CUDA_TRY(cudaGetDevice(&dev));
+  RA_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  // mirrored pairs halve the CTA count; keep them only while that still fills two waves
+  prm.mirrored = static_cast<int64_t>(Hq) * n_ranks * pairs >= 2 * static_cast<int64_t>(sms) ? 1 : 0;
+  int64_t items = 0;
+  for (int b = 0; b < num_seqs; ++b) {
+    prm.items_pre[b] = static_cast<int>(items);
+    const int64_t ntp = (ra::ceil_div(prm.c[b], BM) + 1) / 2;
+    items += static_cast<int64_t>(Hq) * ntp * (prm.mirrored ? n_ranks : 2 * n_ranks);
+    RA_REQUIRE(items < (int64_t(1) << 31), "too many work items");
+  }
+  prm.items_pre[num_seqs] = static_cast<int>(items);
+  const float sc = scale > 0.f ? scale : 1.f / sqrtf(static_cast<float>(d));
+  prm.scale_log2 = sc * 1.4426950408889634f;
+  prm.o = static_cast<__nv_bfloat16*>(o); prm.lse = lse;
+  prm.wait_limit = ra::wait_limit();
+  if (d == 128) return launch_varlen<128>(q, k, v, G, prm, items, stream);
+  return launch_varlen<64>(q, k, v, G, prm, items, stream);
 }
 
 extern "C" ra_status ra_ring_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int32_t B,

@@ -33,6 +33,8 @@ SIGNATURES = {
                          _c.c_int, _vp],
     "ra_ring_attn_fwd_ex": [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _c.c_int, _i32, _i32, _f32,
                             _c.c_int, _i32, _vp],
+    "ra_ring_attn_fwd_varlen": [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _c.c_int, _i32, _i32, _f32,
+                                _vp],
     "ra_ring_schedule_counts": [_i32, _i32, _i32, _vp, _vp],
     "ra_ring_schedule_counts_ex": [_i32, _i32, _i32, _i32, _vp, _vp],
     "ra_lse_merge": [_vp, _vp, _i32, _i64, _i32, _i32, _vp, _c.c_int, _vp, _vp],
@@ -204,6 +206,27 @@ def ring_schedule_counts(S: int, n_ranks: int, causal: bool, kv_tile: int = 128,
     out = torch.empty((n_ranks, 3), dtype=torch.int64, device=device)
     _check(lib().ra_ring_schedule_counts_ex(S, n_ranks, 1 if causal else 0, kv_tile, _ptr(out), _stream()))
     return out
+
+
+def ring_attn_fwd_varlen(q, k, v, seq_lens: Sequence[int], causal: bool, n_ranks: int,
+                         scale: Optional[float] = None, o=None, lse=None):
+    """Ring-order attention over requests of different lengths, on the head-tail gathered layout
+    (``zigzag_partition(seq_lens, n_ranks)`` then ``gather_rows``).  q [G, Hq, d], k/v [G, Hkv, d]
+    bf16 with G the padded total; returns (O [G, Hq, d], LSE float32 [G, Hq]) in the same order."""
+    _need_cuda(q, k, v, o, lse)
+    rows, Hq, d = q.shape
+    n = len(seq_lens)
+    G = sum(-(-int(L) // (2 * n_ranks)) * 2 * n_ranks for L in seq_lens)
+    if rows != G or k.shape[0] != G or v.shape[0] != G:
+        raise ValueError("q, k, v must have the %d rows of the padded gathered layout" % G)
+    arr = (_i64 * max(n, 1))(*[int(x) for x in seq_lens])
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((rows, Hq), dtype=torch.float32, device=q.device)
+    _check(lib().ra_ring_attn_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), arr, n, Hq, k.shape[1], d,
+                                         _dt(q), 1 if causal else 0, n_ranks, float(scale or 0.0), _stream()))
+    return o, lse
 
 
 def attn_block_fwd(q, k, v, q_pos0: int, k_pos0: int, causal: bool, scale: Optional[float] = None,

@@ -159,6 +159,35 @@ ra_status ra_ring_attn_fwd(const void* q, const void* k, const void* v, void* o,
                            ra_dtype dt, int32_t causal, int32_t n_ranks, float scale,
                            ra_layout layout, ra_stream stream);
 
+/* ------------------------------------------------------------------------
+ * ra_ring_attn_fwd_varlen -- ring-order attention over several requests of
+ * different lengths in one call, on the layout the head-tail partition
+ * gathers them to (ra_zigzag_partition + ra_gather_rows with the same
+ * seq_lens and n_ranks).
+ * Sources: as ra_ring_attn_fwd; vLLM-Ascend developer guide "Context
+ * Parallel (CP)", PCP head-tail token partition (each request padded to a
+ * multiple of 2*pcp, its parts paired first-with-last, the gathered buffer
+ * rank-major over requests).
+ *
+ * seq_lens  host int64 [num_seqs] real lengths L_b >= 0 (1 <= num_seqs <= 256).
+ *           Request b is padded to L'_b = ceil(L_b/2N)*2N and cut into chunks
+ *           of c_b = L'_b/2N tokens.
+ * q, k, v   device bf16 [G, Hq|Hkv, d], G = sum_b L'_b rows in gathered order:
+ *           rank-major, then request, then chunk r and chunk 2N-1-r of it.
+ * o, lse    device out, same row order ([G, Hq, d] bf16 and [G, Hq] fp32).
+ *           Rows of padding positions get the attention of a query at that
+ *           position (the restore index drops them).
+ * Each request attends to its own keys only; keys at padding positions
+ * (>= L_b) are masked; causal compares original positions.  Runs the
+ * adjacent-tile tcgen05 kernel (any Hq/Hkv); reads the device's SM count.
+ * Errors: as ra_ring_attn_fwd; RA_ERR_UNSUPPORTED for RA_F32 or d not in
+ * {64, 128}; a total padded length >= 2^31 is RA_ERR_INVALID_ARG.
+ * ---------------------------------------------------------------------- */
+ra_status ra_ring_attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                                  const int64_t* seq_lens, int32_t num_seqs, int32_t Hq, int32_t Hkv,
+                                  int32_t d, ra_dtype dt, int32_t causal, int32_t n_ranks, float scale,
+                                  ra_stream stream);
+
 /* Same as ra_ring_attn_fwd with an explicit bf16 kernel variant:
  * 0 = automatic (2 when Hq/Hkv is even, else 3);
  * 1 = one query head per CTA (mirrored pair of query tiles, 128-key tiles,

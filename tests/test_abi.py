@@ -114,6 +114,23 @@ def test_merge_validation(ra):
     assert _call(ra, "ra_lse_merge", p, p, 2, 4, 2, 6, p, 0, p, None) == ra.RA_ERR_UNSUPPORTED
 
 
+def test_varlen_validation(ra):
+    p = ctypes.c_void_p(1 << 20)
+
+    def run(lens, n=None, dt=1, d=128, Hq=4, Hkv=2, N=2):
+        arr = (ctypes.c_int64 * max(len(lens), 1))(*lens)
+        return _call(ra, "ra_ring_attn_fwd_varlen", p, p, p, p, p, arr, len(lens) if n is None else n, Hq, Hkv, d, dt,
+                     1, N, ctypes.c_float(0.0), None)
+
+    assert run([8, 4], n=0) == ra.RA_ERR_INVALID_ARG
+    assert run([8] * 257) == ra.RA_ERR_INVALID_ARG and "num_seqs" in ra.last_error()
+    assert run([8, -1]) == ra.RA_ERR_INVALID_ARG and "negative" in ra.last_error()
+    assert run([8], dt=0) == ra.RA_ERR_UNSUPPORTED
+    assert run([8], d=96) == ra.RA_ERR_UNSUPPORTED
+    assert run([8], Hq=3) == ra.RA_ERR_INVALID_ARG
+    assert run([0, 0]) == ra.RA_OK                          # nothing to do, nothing launched
+
+
 def test_rope_gather_validation(ra):
     p = ctypes.c_void_p(1 << 20)
     q = ctypes.c_void_p(1 << 24)

@@ -206,6 +206,36 @@ def test_bf16_adjacent_tiles_mirrored_ragged(ra, S, N, Hq, Hkv):
     _check_sampled(o, lse, seed, 0, S, Hq, Hkv, d, rows)
 
 
+@pytest.mark.parametrize("lens,N,Hq,Hkv,d,causal", [
+    ([300, 0, 1, 1000, 77], 2, 4, 2, 128, True),     # padding in most requests, an empty and a 1-token one
+    ([300, 0, 1, 1000, 77], 2, 3, 1, 128, False),    # non-causal: padding keys must be masked
+    ([129, 257, 1], 3, 2, 1, 64, True),
+    ([4096, 2048, 3000, 100], 4, 32, 8, 128, True),  # enough work for mirrored tile pairs
+])
+def test_varlen_ring_matches_per_request_attention(ra, lens, N, Hq, Hkv, d, causal):
+    """Several requests of different lengths in one call on the head-tail gathered layout;
+    after the restore every request equals its own full attention."""
+    T = sum(lens)
+    q = I.synth_normal(31, I.TID_Q, (T, Hq, d), torch.bfloat16)
+    k = I.synth_normal(31, I.TID_K, (T, Hkv, d), torch.bfloat16)
+    v = I.synth_normal(31, I.TID_V, (T, Hkv, d), torch.bfloat16)
+    dev = torch.device("cuda")
+    perm, restore = ra.zigzag_partition(lens, N)
+    qz, kz, vz = (ra.gather_rows(x.to(dev), perm) for x in (q, k, v))
+    oz, lz = ra.ring_attn_fwd_varlen(qz, kz, vz, lens, causal, N)
+    o, lse = ra.gather_rows(oz, restore), ra.gather_rows(lz, restore)
+    check_status(ra)
+    Os, Ls = [], []
+    start = 0
+    for L in lens:
+        if L:
+            O, Lr = oracle.full_attention(q[start:start + L], k[start:start + L], v[start:start + L], causal)
+            Os.append(O)
+            Ls.append(Lr)
+        start += L
+    assert_parity(o, np.concatenate(Os), lse, np.concatenate(Ls), torch.bfloat16, "varlen %s" % lens)
+
+
 def test_bf16_long_context_131k(ra):
     """B=1, Hq=32, Hkv=8, S=131072, d=128, causal, N=16 (32 chunks of 4096); sampled rows."""
     B, S, Hq, Hkv, d, N, seed = 1, 131072, 32, 8, 128, 16, 5
