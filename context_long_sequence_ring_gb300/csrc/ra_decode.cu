@@ -464,9 +464,17 @@ extern "C" ra_status ra_cp_decode(const void* q, const void* k_cache, const void
 // array (kNoAllocScratchBytes) until the process exits.
 //
 // The array's name is a host-side stand-in in host code, not a device
-// address; its device address is looked up once per device (with that device
-// current) by cudaGetSymbolAddress, the first time the entry point runs on
-// that device, and then reused.
+// address; its device address is looked up with cudaGetSymbolAddress (with the
+// device current) the first time the entry point runs on a device, and reused
+// while that device's CUDA context stays the same.  A context that was torn
+// down and created again (cudaDeviceReset, for one) reloads this module, which
+// may place the array elsewhere, so the address is looked up again then.
+//
+// Under lazy module loading (CUDA's default) this module, and with it the
+// array, is loaded by the first call on each device: that call commits the
+// array's device memory.  Callers that must not allocate after start-up make
+// one warm-up call per device at start-up (the same call that must precede any
+// stream capture), or load modules eagerly (CUDA_MODULE_LOADING=EAGER).
 //
 // All calls share the array and it keeps the last call's contents.  Nothing in
 // it has to start at zero: each call writes the LSE of every partial before the
@@ -481,18 +489,48 @@ namespace {
 constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mutex;
 void* g_scratch_ptr[kMaxDevices] = {};
+unsigned long long g_scratch_ctx_id[kMaxDevices] = {};  // id of the context the address belongs to
 
-// Device address of g_decode_scratch on the current device (looked up once).
+// cuCtxGetCurrent and cuCtxGetId from the driver (the library links the
+// runtime only).  A context id is unique for the life of the process, so a
+// context created again after a reset has a new one.
+using CtxGetCurrentFn = int (*)(void**);
+using CtxGetIdFn = int (*)(void*, unsigned long long*);
+template <class Fn>
+Fn driver_fn(const char* name) {
+  void* ptr = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &ptr, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+      q == cudaDriverEntryPointSuccess)
+    return reinterpret_cast<Fn>(ptr);
+  return nullptr;
+}
+
+// Id of the calling thread's current context, 0 if none is current yet.
+unsigned long long current_ctx_id() {
+  static const CtxGetCurrentFn get_ctx = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent");
+  static const CtxGetIdFn get_id = driver_fn<CtxGetIdFn>("cuCtxGetId");
+  void* ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_ctx || !get_id || get_ctx(&ctx) != 0 || ctx == nullptr || get_id(ctx, &id) != 0) return 0;
+  return id;
+}
+
+// Device address of g_decode_scratch in the current device's context: looked
+// up (with that device current) the first time on a device, and again
+// whenever the device's context has changed since.
 ra_status scratch_address(void** out) {
   int dev = 0;
   RA_CUDA_TRY(cudaGetDevice(&dev));
   if (dev < 0 || dev >= kMaxDevices) return ra::fail(RA_ERR_UNSUPPORTED, "device index %d out of range", dev);
   std::lock_guard<std::mutex> lock(g_scratch_mutex);
-  if (g_scratch_ptr[dev] == nullptr) {
+  const unsigned long long id = current_ctx_id();
+  if (g_scratch_ptr[dev] == nullptr || id == 0 || id != g_scratch_ctx_id[dev]) {
     void* ptr = nullptr;
     const cudaError_t e = cudaGetSymbolAddress(&ptr, g_decode_scratch);
     if (e != cudaSuccess) return ra::cuda_status(e, "cudaGetSymbolAddress(decode scratch)");
     g_scratch_ptr[dev] = ptr;
+    g_scratch_ctx_id[dev] = current_ctx_id();  // the lookup made the primary context current
   }
   *out = g_scratch_ptr[dev];
   return RA_OK;

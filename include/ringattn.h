@@ -384,13 +384,19 @@ ra_status ra_cp_decode(const void* q, const void* k_cache, const void* v_cache,
  * Same arguments and results as ra_cp_decode, without workspace/ws_bytes:
  * the fp32 partials go to a fixed 32 MiB scratch array inside the library's
  * device memory, which every GPU that loads the library holds until exit.
- * Nothing is allocated and no allocating routine is called.
+ * No call allocates device memory through cudaMalloc, cudaFree or an
+ * allocating library routine.
+ * - The first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress, with that device current) and caches it for that
+ *   device's context (a context created again after a reset is looked up
+ *   again).  Under lazy module loading, CUDA's default, that first call also
+ *   loads the decode module and so commits the array's 32 MiB; a caller that
+ *   may not allocate after start-up makes one warm-up call per device at
+ *   start-up, or runs with CUDA_MODULE_LOADING=EAGER.  Calls after the first
+ *   commit nothing.  Make the first call before any stream capture.
  * - A decode whose partials need more than 32 MiB
  *   (ra_cp_decode_workspace_size) is rejected with RA_ERR_INVALID_ARG; a
  *   larger split_blocks makes it smaller.
- * - The first call on a device looks up the array's device address
- *   (cudaGetSymbolAddress, with that device current) and caches it; make that
- *   first call before any stream capture.
  * - All calls share the array and it keeps the last call's contents.  Nothing
  *   in it needs to start at zero (every partial's LSE is written before it is
  *   read, and a partial's O is read only if the same call wrote it).  Calls

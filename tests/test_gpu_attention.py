@@ -236,16 +236,47 @@ def test_varlen_ring_matches_per_request_attention(ra, lens, N, Hq, Hkv, d, caus
     assert_parity(o, np.concatenate(Os), lse, np.concatenate(Ls), torch.bfloat16, "varlen %s" % lens)
 
 
+def _long_context_rows(S, N, rng, n_random):
+    """Rows checked at S=131072: the first and last row of query tiles 0, 1, nt/2-1, nt/2, nt-2 and
+    nt-1 of every one of the 2N chunks (so both tiles of several mirrored pairs: tile j of chunk r
+    runs with tile nt-1-j of chunk 2N-1-r), plus n_random seeded rows."""
+    c = S // (2 * N)
+    nt = -(-c // 128)
+    rows = set()
+    for ch in range(2 * N):
+        for j in sorted({0, 1, nt // 2 - 1, nt // 2, nt - 2, nt - 1}):
+            lo = ch * c + j * 128
+            rows.update((lo, min(lo + 127, ch * c + c - 1)))
+    rows.update(rng.integers(0, S, size=n_random).tolist())
+    return np.array(sorted(rows))
+
+
 def test_bf16_long_context_131k(ra):
-    """B=1, Hq=32, Hkv=8, S=131072, d=128, causal, N=16 (32 chunks of 4096); sampled rows."""
+    """B=1, Hq=32, Hkv=8, S=131072, d=128, causal, N=16 (32 chunks of 4096), in the launch
+    configuration the benchmark times: head-tail partition, gather to the ranks' layout, ring
+    attention on the zigzag layout, restore.  Checked on tile-boundary rows of all 32 chunks
+    and 256 random rows."""
     B, S, Hq, Hkv, d, N, seed = 1, 131072, 32, 8, 128, 16, 5
     q, k, v = _device_inputs(ra, seed, B, S, Hq, Hkv, d)
-    o, lse = ra.ring_attn_fwd(q, k, v, True, N, B=B)
+    perm, restore = ra.zigzag_partition([S] * B, N)
+    qz, kz, vz = (ra.gather_rows(x, perm) for x in (q, k, v))
+    oz, lz = ra.ring_attn_fwd(qz, kz, vz, True, N, B=B, layout="zigzag")
+    o, lse = ra.gather_rows(oz, restore), ra.gather_rows(lz, restore)
     check_status(ra)
-    rng = np.random.default_rng(55)
-    rows = _sample_rows(S, N, S // (2 * N), rng, 16)
-    rows = np.concatenate([rows[::3], [0, S - 1]])
-    _check_sampled(o, lse, seed, 0, S, Hq, Hkv, d, np.unique(rows))
+    rows = _long_context_rows(S, N, np.random.default_rng(55), 256)
+    kk = I.synth_rows(seed, I.TID_K, np.arange(S), Hkv * d, torch.bfloat16).reshape(S, Hkv, d).double().numpy()
+    vv = I.synth_rows(seed, I.TID_V, np.arange(S), Hkv * d, torch.bfloat16).reshape(S, Hkv, d).double().numpy()
+    c = S // (2 * N)
+    O = np.zeros((len(rows), Hq, d))
+    L = np.zeros((len(rows), Hq))
+    for ch in range(2 * N):      # a causal row of chunk ch sees keys before (ch+1)*c only
+        sel = np.nonzero((rows >= ch * c) & (rows < (ch + 1) * c))[0]
+        if len(sel):
+            qr = I.synth_rows(seed, I.TID_Q, rows[sel], Hq * d, torch.bfloat16).reshape(len(sel), Hq, d)
+            O[sel], L[sel] = oracle.attention_rows(qr, rows[sel], kk[:(ch + 1) * c], vv[:(ch + 1) * c], True)
+    idx = torch.as_tensor(rows, device=o.device)
+    assert len(rows) >= 384 + 200
+    assert_parity(o[idx], O, lse[idx], L, torch.bfloat16, "S=131072 sampled rows")
 
 
 # --------------------------------------------------------------------- block partials and segmented prefill

@@ -58,6 +58,42 @@ def test_noalloc_decode_matches_workspace_decode_on_consecutive_calls():
         assert (lse - l_ref).abs().max().item() <= tol["lse"], "call %d: LSE" % call
 
 
+def test_noalloc_decode_after_a_larger_call_with_another_split():
+    # A large decode leaves its partials in the shared scratch; a smaller one with another split
+    # reads only what it wrote itself, so the stale contents must not leak into its result.
+    ra = ra_lib()
+    bs, I_, pcp, dcp, Hq, Hkv, d = 64, 16, 2, 2, 8, 2, 128
+    tol = TOL[torch.bfloat16]
+    big = _cache(ra, 23, 12, 3000, 20000, bs, I_, pcp, dcp, Hkv, d)
+    small = _cache(ra, 24, 3, 100, 2500, bs, I_, pcp, dcp, Hkv, d)
+    for (kc, vc, bt, ctx), R, split, seed in ((big, 12, 1, 41), (small, 3, 3, 42), (big, 12, 2, 43)):
+        assert ra.cp_decode_workspace_size(R, Hq, d, bt.shape[1], pcp, dcp, split) <= 32 << 20
+        q = I.synth_normal(seed, I.TID_Q, (R, Hq, d), torch.bfloat16).to(DEV)
+        o_ref, l_ref = ra.cp_decode(q, kc, vc, bt, ctx, I_, pcp, dcp, split_blocks=split)
+        o, lse = ra.cp_decode_noalloc(q, kc, vc, bt, ctx, I_, pcp, dcp, split_blocks=split)
+        check_status(ra)
+        e = (o.float() - o_ref.float()).abs()
+        assert e.max().item() <= tol["o_max"] and e.mean().item() <= tol["o_mean"], "R=%d split=%d" % (R, split)
+        assert (lse - l_ref).abs().max().item() <= tol["lse"], "R=%d split=%d" % (R, split)
+
+
+def test_warm_noalloc_call_commits_no_device_memory():
+    ra = ra_lib()
+    R, bs, I_, pcp, dcp, Hq, Hkv, d, split = 4, 64, 16, 2, 2, 8, 2, 128, 2
+    kc, vc, bt, ctx = _cache(ra, 25, R, 500, 5000, bs, I_, pcp, dcp, Hkv, d)
+    q = I.synth_normal(44, I.TID_Q, (R, Hq, d), torch.bfloat16).to(DEV)
+    o = torch.empty((R, Hq, d), dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty((R, Hq), dtype=torch.float32, device=DEV)
+    ra.cp_decode_noalloc(q, kc, vc, bt, ctx, I_, pcp, dcp, split_blocks=split, o=o, lse=lse)   # warm-up call
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    for _ in range(3):
+        ra.cp_decode_noalloc(q, kc, vc, bt, ctx, I_, pcp, dcp, split_blocks=split, o=o, lse=lse)
+    torch.cuda.synchronize()
+    check_status(ra)
+    assert torch.cuda.mem_get_info()[0] == free0, "a warm call changed the device's free memory"
+
+
 def test_noalloc_decode_rejects_a_decode_larger_than_its_scratch():
     ra = ra_lib()
     R, Hq, Hkv, d, bs, I_, pcp, dcp = 2, 32, 8, 128, 64, 16, 2, 4
