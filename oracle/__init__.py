@@ -37,18 +37,19 @@ invariants and brute force on tiny inputs).
 """
 
 from .attention import (full_attention, attention_rows, attention_block, segmented_attention,
-                        ring_attention, ring_partials, lse_merge, rank_chunks,
+                        ring_attention, ring_partials, ring_step, lse_merge, rank_chunks,
                         causal_pairs_per_rank, causal_tiles_per_rank)
 from .partition import zigzag_partition, gather_rows
 from .rope import rope_theta, rope_cos_sin, rotate_half, apply_rope, rope_gather
 from .kvcache import (cp_slot_mapping, cp_token_location, cp_kv_scatter, cp_kv_gather,
-                      cp_decode, cp_decode_partials, decode_reference)
+                      cp_decode, cp_decode_partials, cp_lse_ag_out_rs, decode_reference)
 
 __all__ = [
     "full_attention", "attention_rows", "attention_block", "segmented_attention",
-    "ring_attention", "ring_partials",
+    "ring_attention", "ring_partials", "ring_step",
     "lse_merge", "rank_chunks", "causal_pairs_per_rank", "causal_tiles_per_rank",
     "zigzag_partition", "gather_rows", "cp_slot_mapping", "cp_token_location",
-    "cp_kv_scatter", "cp_kv_gather", "cp_decode", "cp_decode_partials", "decode_reference",
+    "cp_kv_scatter", "cp_kv_gather", "cp_decode", "cp_decode_partials", "cp_lse_ag_out_rs",
+    "decode_reference",
     "rope_theta", "rope_cos_sin", "rotate_half", "apply_rope", "rope_gather",
 ]

@@ -244,6 +244,40 @@ def ring_partials(q, k, v, causal: bool, n_ranks: int, scale=None):
     return parts, pos
 
 
+def ring_step(q_local, k_held, v_held, n_ranks: int, rank: int, src: int, causal: bool,
+              o_in=None, lse_in=None, B: int = 1, scale=None):
+    """One ring step of one rank, applied to that rank's running result.
+
+    The rank's local buffers are what the head-tail partition gives it: per
+    sequence (B of them, equal length 2Nc), chunk `rank` followed by chunk
+    2N-1-rank, c rows each.  q_local [B*2c, Hq, d] are rank `rank`'s queries;
+    k_held, v_held [B*2c, Hkv, d] are the K/V block that rank holds at this
+    step, i.e. the local K/V of rank `src` (src = (rank - t) mod N at step t,
+    "Ring Attention" tag page, ring topology).  The partial (O_p, LSE_p) of the
+    queries over the visible keys of that block comes from the definition;
+    it is then folded into the running (o_in, lse_in) with the LSE merge (the
+    blockwise decomposition of the same page: a partial over a key subset is
+    carried by its LSE).  Without o_in the partial itself is the result.
+    Returns (O [B*2c, Hq, d], LSE [B*2c, Hq]).
+    """
+    q_local, k_held, v_held = _as64(q_local), _as64(k_held), _as64(v_held)
+    N = int(n_ranks)
+    rows = q_local.shape[0]
+    if rows % (2 * B) != 0 or k_held.shape[0] != rows:
+        raise ValueError("local buffers must hold B sequences of 2c rows")
+    c = rows // (2 * B)
+    qpos = _rank_positions(N, c, rank)
+    kpos = _rank_positions(N, c, src)
+    O_p = np.zeros(q_local.shape)
+    L_p = np.zeros(q_local.shape[:2])
+    for b in range(B):
+        sl = slice(b * 2 * c, (b + 1) * 2 * c)
+        O_p[sl], L_p[sl] = _rows_over_keys(q_local[sl], qpos, k_held[sl], v_held[sl], kpos, causal, scale)
+    if o_in is None:
+        return O_p, L_p
+    return lse_merge(np.stack([_as64(o_in), O_p]), np.stack([_as64(lse_in), L_p]))
+
+
 def _rows_over_keys(qr, qpos, kk, vv, kpos, causal, scale):
     qr, kk, vv = _as64(qr), _as64(kk), _as64(vv)
     n, Hq, d = qr.shape

@@ -175,6 +175,45 @@ def cp_decode(q, k_cache, v_cache, block_table, ctx_lens, block_size, interleave
     return lse_merge(O_p, L_p)
 
 
+def cp_lse_ag_out_rs(o_dev, lse_dev):
+    """The decode's merge across W devices, in the steps the name spells out
+    (vLLM-Ascend "Context Parallel (CP)", DCP decode: cp_lse_ag_out_rs; the
+    weights are those of the blockwise decomposition on the "Ring Attention"
+    tag page).  Device w holds its own partial O_w [R, Hq, d] (normalised over
+    the keys it stores) and LSE_w [R, Hq].
+      1. all-gather the LSEs, so every device sees LSE_0 .. LSE_{W-1};
+      2. every device rescales its own O_w by e^{LSE_w - LSE} with
+         LSE = ln sum_w e^{LSE_w} (a device with LSE_w = -inf contributes 0);
+      3. reduce-scatter the rescaled outputs over the head dimension: the sum
+         over devices, of which device w keeps heads [w*Hq/W, (w+1)*Hq/W).
+    Requires Hq % W == 0.  Returns a list over devices of (O [R, Hq/W, d],
+    LSE [R, Hq/W]).
+    """
+    W = len(o_dev)
+    o_dev = [_as64(o) for o in o_dev]
+    lse_dev = [_as64(l) for l in lse_dev]
+    R, Hq, d = o_dev[0].shape
+    if Hq % W != 0:
+        raise ValueError("Hq must be a multiple of the number of devices")
+    hs = Hq // W
+    gathered = np.stack(lse_dev)                                   # step 1: [W, R, Hq] on every device
+    M = gathered.max(axis=0)
+    live = np.isfinite(M)
+    Ms = np.where(live, M, 0.0)
+    tot = np.where(np.isfinite(gathered), np.exp(gathered - Ms[None]), 0.0).sum(axis=0)
+    LSE = np.where(live, Ms + np.log(np.where(live, tot, 1.0)), NEG_INF)
+    scaled = []
+    for w in range(W):                                             # step 2, on device w
+        wgt = np.where(np.isfinite(lse_dev[w]) & live, np.exp(lse_dev[w] - np.where(live, LSE, 0.0)), 0.0)
+        o_safe = np.where(np.isfinite(lse_dev[w])[..., None], o_dev[w], 0.0)
+        scaled.append(wgt[..., None] * o_safe)
+    out = []
+    for w in range(W):                                             # step 3: device w's share of the sum
+        heads = slice(w * hs, (w + 1) * hs)
+        out.append((sum(x[:, heads] for x in scaled), LSE[:, heads]))
+    return out
+
+
 def decode_reference(q_row, k_tokens, v_tokens, scale=None):
     """Plain attention of one query [Hq, d] over a request's own token K/V
     [L, Hkv, d] (no cache involved): the value the sharded decode must reach."""
@@ -184,4 +223,4 @@ def decode_reference(q_row, k_tokens, v_tokens, scale=None):
 
 
 __all__ = ["cp_token_location", "cp_slot_mapping", "cp_kv_scatter", "cp_kv_gather",
-           "cp_decode_partials", "cp_decode", "decode_reference"]
+           "cp_decode_partials", "cp_decode", "cp_lse_ag_out_rs", "decode_reference"]

@@ -323,3 +323,78 @@ def test_attention_block_rows_before_every_key_are_empty():
     assert np.all(np.isneginf(L[:3])) and np.all(O[:3] == 0)
     np.testing.assert_allclose(O[3], v[0, [0, 0]], atol=1e-15)
     np.testing.assert_allclose(L[3], 0.5 * np.einsum("hd,hd->h", q[3], k[0, [0, 0]]), atol=1e-14)
+
+
+# ---------------------------------------------------------------- one ring step of one rank
+
+def _local(x, N, c, r, B):
+    """Rank r's local rows of a [B*S, ...] natural-order array: per sequence chunk r, then 2N-1-r."""
+    S = 2 * N * c
+    idx = np.concatenate([b * S + np.concatenate([np.arange(ch * c, ch * c + c) for ch in oracle.rank_chunks(N, r)])
+                          for b in range(B)])
+    return x[idx], idx
+
+
+@pytest.mark.parametrize("N,c,B", [(1, 3, 1), (2, 3, 1), (3, 2, 2), (4, 2, 1)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_ring_steps_of_a_rank_equal_full_attention(N, c, B, causal):
+    # steps t = 0..N-1 on the block of rank (r - t) mod N reach the rank's rows of full attention
+    rng = np.random.default_rng(100 + N * 10 + c + B)
+    S = 2 * N * c
+    q, k, v = _rand(rng, B * S, 4, 2, 8)
+    for r in range(N):
+        ql, rows = _local(q, N, c, r, B)
+        O = L = None
+        for t in range(N):
+            s = (r - t) % N
+            kl, _ = _local(k, N, c, s, B)
+            vl, _ = _local(v, N, c, s, B)
+            O, L = oracle.ring_step(ql, kl, vl, N, r, s, causal, O, L, B=B)
+        for b in range(B):
+            Of, Lf = oracle.full_attention(q[b * S:(b + 1) * S], k[b * S:(b + 1) * S], v[b * S:(b + 1) * S], causal)
+            sel = slice(b * 2 * c, (b + 1) * 2 * c)
+            np.testing.assert_allclose(O[sel], Of[rows[sel] - b * S], atol=1e-12)
+            np.testing.assert_allclose(L[sel], Lf[rows[sel] - b * S], atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_ring_steps_in_any_order(causal):
+    rng = np.random.default_rng(120)
+    N, c = 3, 2
+    q, k, v = _rand(rng, 2 * N * c, 2, 1, 4)
+    O_full, L_full = oracle.full_attention(q, k, v, causal)
+    for r in range(N):
+        ql, rows = _local(q, N, c, r, 1)
+        for order in itertools.permutations(range(N)):
+            O = L = None
+            for s in order:
+                O, L = oracle.ring_step(ql, _local(k, N, c, s, 1)[0], _local(v, N, c, s, 1)[0], N, r, s, causal, O, L)
+            np.testing.assert_allclose(O, O_full[rows], atol=1e-12)
+            np.testing.assert_allclose(L, L_full[rows], atol=1e-12)
+
+
+def test_ring_step_first_row_sees_only_its_own_key():
+    # N=2, c=1, S=4: rank 0 holds positions (0, 3), rank 1 holds (1, 2).  Under the causal mask the
+    # query at position 0 sees no key of rank 1's block (LSE -inf, O 0) and only key 0 of its own.
+    q = np.array([[[1.0]], [[2.0]], [[0.5]], [[1.5]]])
+    k = np.array([[[0.3]], [[1.0]], [[-1.0]], [[2.0]]])
+    v = np.array([[[10.0]], [[20.0]], [[30.0]], [[40.0]]])
+    ql, _ = _local(q, 2, 1, 0, 1)
+    O1, L1 = oracle.ring_step(ql, _local(k, 2, 1, 1, 1)[0], _local(v, 2, 1, 1, 1)[0], 2, 0, 1, True)
+    assert L1[0, 0] == -np.inf and O1[0, 0, 0] == 0.0
+    # row 1 (position 3) sees keys 1 and 2 of the held block: scores 1.5*1.0 and 1.5*(-1.0) at scale 1
+    e1, e2 = np.exp(1.5), np.exp(-1.5)
+    assert O1[1, 0, 0] == pytest.approx((20 * e1 + 30 * e2) / (e1 + e2), abs=1e-12)
+    assert L1[1, 0] == pytest.approx(np.log(e1 + e2), abs=1e-12)
+    O0, L0 = oracle.ring_step(ql, _local(k, 2, 1, 0, 1)[0], _local(v, 2, 1, 0, 1)[0], 2, 0, 0, True)
+    assert O0[0, 0, 0] == pytest.approx(10.0) and L0[0, 0] == pytest.approx(1.0 * 0.3)
+
+
+def test_planted_held_block_positions_are_caught(monkeypatch):
+    # a step that took the held block's keys to sit at the rank's own positions must fail the identity
+    import oracle.attention as A
+    real = A._rows_over_keys
+    monkeypatch.setattr(A, "_rows_over_keys",
+                        lambda qr, qpos, kk, vv, kpos, causal, scale: real(qr, qpos, kk, vv, qpos, causal, scale))
+    with pytest.raises(AssertionError):
+        test_ring_steps_of_a_rank_equal_full_attention(2, 3, 1, True)

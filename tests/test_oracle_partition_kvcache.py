@@ -169,3 +169,73 @@ def test_kv_gather_reorders_requests():
     s2 = int(c["qsl"][2])
     np.testing.assert_array_equal(k2, c["k"][s2:s2 + n2][::-1])
     np.testing.assert_array_equal(v2, c["v"][s2:s2 + n2][::-1])
+
+
+# ---------------------------------------------------------------- cp_lse_ag_out_rs across devices
+
+def test_cp_lse_ag_out_rs_hand_worked():
+    # W=2 devices, R=1, Hq=2, d=1.  Head 0: LSEs 0 and ln 3 -> weights 1:3; head 1: ln 3 and 0 -> 3:1.
+    o = [np.array([[[1.0], [2.0]]]), np.array([[[3.0], [8.0]]])]
+    lse = [np.array([[0.0, np.log(3.0)]]), np.array([[np.log(3.0), 0.0]])]
+    (O0, L0), (O1, L1) = oracle.cp_lse_ag_out_rs(o, lse)
+    assert O0.shape == (1, 1, 1) and O1.shape == (1, 1, 1)
+    assert O0[0, 0, 0] == pytest.approx((1 * 1.0 + 3 * 3.0) / 4, abs=1e-14)     # device 0 keeps head 0
+    assert O1[0, 0, 0] == pytest.approx((3 * 2.0 + 1 * 8.0) / 4, abs=1e-14)     # device 1 keeps head 1
+    assert L0[0, 0] == pytest.approx(np.log(4.0), abs=1e-14) and L1[0, 0] == pytest.approx(np.log(4.0), abs=1e-14)
+
+
+@pytest.mark.parametrize("W", [1, 2, 4])
+def test_cp_lse_ag_out_rs_equals_the_merge_over_devices(W):
+    rng = np.random.default_rng(200 + W)
+    R, Hq, d = 3, 8, 5
+    o = [rng.standard_normal((R, Hq, d)) for _ in range(W)]
+    lse = [rng.standard_normal((R, Hq)) * 3 for _ in range(W)]
+    lse[0][1, 2] = -np.inf                       # a device with no key for one (request, head)
+    if W > 1:
+        for w in range(W):
+            lse[w][2, 5] = -np.inf               # nobody has a key: O 0, LSE -inf
+    O, L = oracle.lse_merge(np.stack(o), np.stack(lse))
+    out = oracle.cp_lse_ag_out_rs(o, lse)
+    np.testing.assert_allclose(np.concatenate([x[0] for x in out], axis=1), O, atol=1e-13)
+    np.testing.assert_array_equal(np.concatenate([x[1] for x in out], axis=1), L)
+
+
+def test_cp_lse_ag_out_rs_of_device_partials_is_plain_decode():
+    # per device: merge of its split partials; across devices: the collective -> plain attention
+    rng = np.random.default_rng(210)
+    R, Hq, Hkv, d, bs, I_, pcp, dcp = 2, 4, 2, 8, 8, 4, 2, 1
+    W = pcp * dcp
+    lens = [37, 70]
+    T = sum(lens)
+    kt = rng.standard_normal((T, Hkv, d))
+    vt = rng.standard_normal((T, Hkv, d))
+    q = rng.standard_normal((R, Hq, d))
+    vbs = bs * W
+    nvb = [-(-L // vbs) for L in lens]
+    bt = np.full((R, max(nvb)), -1)
+    ids = rng.permutation(sum(nvb))
+    bt[0, :nvb[0]], bt[1, :nvb[1]] = ids[:nvb[0]], ids[nvb[0]:]
+    qsl = np.array([0, lens[0], T])
+    pos = np.concatenate([np.arange(L) for L in lens])
+    slot = oracle.cp_slot_mapping(qsl, pos, bt, bs, I_, pcp, dcp)
+    kc = np.zeros((W, sum(nvb), Hkv, bs, d))
+    vc = np.zeros_like(kc)
+    oracle.cp_kv_scatter(kt, vt, slot, kc, vc, bs)
+    Op, Lp, ns = oracle.cp_decode_partials(q, kc, vc, bt, np.array(lens), bs, I_, pcp, dcp, split_blocks=1)
+    dev = [oracle.lse_merge(Op[w * ns:(w + 1) * ns], Lp[w * ns:(w + 1) * ns]) for w in range(W)]
+    out = oracle.cp_lse_ag_out_rs([x[0] for x in dev], [x[1] for x in dev])
+    O = np.concatenate([x[0] for x in out], axis=1)
+    L = np.concatenate([x[1] for x in out], axis=1)
+    for r in range(R):
+        Or, Lr = oracle.decode_reference(q[r], kt[qsl[r]:qsl[r + 1]], vt[qsl[r]:qsl[r + 1]])
+        np.testing.assert_allclose(O[r], Or, atol=1e-12)
+        np.testing.assert_allclose(L[r], Lr, atol=1e-12)
+
+
+def test_planted_head_share_is_caught(monkeypatch):
+    # a device keeping another device's heads must fail the merge identity
+    import oracle.kvcache as K
+    real = K.cp_lse_ag_out_rs
+    monkeypatch.setattr(oracle, "cp_lse_ag_out_rs", lambda o, l: real(o, l)[::-1])
+    with pytest.raises(AssertionError):
+        test_cp_lse_ag_out_rs_equals_the_merge_over_devices(2)
