@@ -294,6 +294,175 @@ def e2e_pipelined(wl, host_in, host_out, steps):
     return e0.elapsed_time(e1)
 
 
+# ---------------------------------------------------------------------------- the step split across ranks
+
+class DistWorkload:
+    """The same step split across the ranks of the job (context parallelism across devices).
+
+    Prefill: the S-token sequence is cut into 2*world chunks by the head-tail partition and rank r
+    holds chunks r and 2*world-1-r of Q, K and V.  The ranks form a ring: at each of the world steps
+    a rank runs one ring-step kernel on the K/V block it holds while NCCL point-to-point copies pass
+    that block to the next rank (double buffering).  Decode: the cache's W = pcp*dcp devices are
+    spread over the ranks (W/world each, device w on rank w // (W/world)); a rank computes the
+    split-KV partials of its devices, merges them, and the ranks combine their results with
+    cp_lse_ag_out_rs (all-gather of the LSEs, rescale kernel, reduce-scatter of the output over
+    heads), so rank r ends with heads [r*Hq/world, (r+1)*Hq/world) of the decode output."""
+
+    def __init__(self, ra, dev, rank, world):
+        from context_long_sequence_ring_gb300 import cp_dist
+        self.ra, self.dev, self.rank, self.world, self.cp = ra, dev, rank, world, cp_dist
+        P, D = PREFILL, DECODE
+        W = D["pcp"] * D["dcp"]
+        if P["B"] != 1 or P["S"] % (2 * world) != 0:
+            raise ValueError("the split prefill needs B=1 and S a multiple of 2*world")
+        if W % world != 0 or D["Hq"] % world != 0:
+            raise ValueError("pcp*dcp (%d) and Hq (%d) must be multiples of the number of ranks (%d)"
+                             % (W, D["Hq"], world))
+        tab = I.normal_table(torch.bfloat16)
+        S, c = P["S"], P["S"] // (2 * world)
+        perm, _ = ra.zigzag_partition([S], world)
+        loc = perm[rank * 2 * c:(rank + 1) * 2 * c].contiguous()
+        for name, tid, H in (("q", I.TID_Q, P["Hq"]), ("k", I.TID_K, P["Hkv"]), ("v", I.TID_V, P["Hkv"])):
+            full = ra.synth_fill(I.tensor_key(P["seed"], tid), tab, (S, H, P["d"]), dev)
+            setattr(self, name, ra.gather_rows(full, loc))
+            del full
+        self.exchange = cp_dist.P2PExchange() if world > 1 else None
+        self.ring_step = ra.ring_step_fn(world, rank, True)
+        # decode: the shards of this rank's devices
+        wl = I.decode_workload(D["seed"], D["R"], D["lo"], D["hi"], D["bs"], D["pcp"], D["dcp"])
+        T = wl["total_tokens"]
+        kt = ra.synth_fill(I.tensor_key(D["seed"], I.TID_K), tab, (T, D["Hkv"], D["d"]), dev)
+        vt = ra.synth_fill(I.tensor_key(D["seed"], I.TID_V), tab, (T, D["Hkv"], D["d"]), dev)
+        ctx = wl["ctx_lens"]
+        qsl = torch.zeros(D["R"] + 1, dtype=torch.int32)
+        qsl[1:] = torch.cumsum(ctx, 0)
+        pos = torch.cat([torch.arange(int(L), dtype=torch.int32) for L in ctx])
+        self.bt = wl["block_table"].to(dev)
+        self.ctx = ctx.to(dev)
+        self.n_dev = W // world
+        self.dev0 = rank * self.n_dev
+        slot = ra.cp_slot_mapping(qsl.to(dev), pos.to(dev), self.bt, D["bs"], D["I"], D["pcp"], D["dcp"])
+        self.kc = torch.empty((self.n_dev, wl["num_blocks"], D["Hkv"], D["bs"], D["d"]), dtype=torch.bfloat16,
+                              device=dev)
+        self.vc = torch.empty_like(self.kc)
+        ra.cp_kv_scatter(kt, vt, slot[self.dev0:self.dev0 + self.n_dev], self.kc, self.vc)
+        last = (qsl[1:] - 1).long()
+        self.new_k = kt[last.to(dev)].contiguous()
+        self.new_v = vt[last.to(dev)].contiguous()
+        del kt, vt, slot
+        self.new_pos = (ctx - 1).to(torch.int32).to(dev)
+        self.new_qsl = torch.arange(D["R"] + 1, dtype=torch.int32, device=dev)
+        self.new_slot = torch.empty((W, D["R"]), dtype=torch.int32, device=dev)
+        self.qd = I.synth_normal(D["seed"], I.TID_Q, (D["R"], D["Hq"], D["d"]), torch.bfloat16).to(dev)
+        self.op, self.lp = ra.cp_decode_partials(self.qd, self.kc, self.vc, self.bt, self.ctx, D["I"], D["pcp"],
+                                                 D["dcp"], dev0=self.dev0, split_blocks=D["split"])
+        self.o_loc = torch.empty((D["R"], D["Hq"], D["d"]), dtype=torch.float32, device=dev)
+        self.l_loc = torch.empty((D["R"], D["Hq"]), dtype=torch.float32, device=dev)
+        self.rescale = ra.cp_lse_rescale_fn()
+        self.ctx_host = ctx
+        self.parts = ("prefill", "decode")
+        torch.cuda.synchronize()
+
+    def step(self, e=None):
+        ra, D = self.ra, DECODE
+        if e: e[0].record()
+        self.o, self.lse = self.cp.ring_attention(self.q, self.k, self.v, step=self.ring_step, exchange=self.exchange,
+                                                  out_dtype=torch.bfloat16)
+        if e: e[1].record()
+        ra.cp_slot_mapping(self.new_qsl, self.new_pos, self.bt, D["bs"], D["I"], D["pcp"], D["dcp"], out=self.new_slot)
+        ra.cp_kv_scatter(self.new_k, self.new_v, self.new_slot[self.dev0:self.dev0 + self.n_dev], self.kc, self.vc)
+        if e: e[2].record()
+        ra.cp_decode_partials(self.qd, self.kc, self.vc, self.bt, self.ctx, D["I"], D["pcp"], D["dcp"],
+                              dev0=self.dev0, split_blocks=D["split"], o_parts=self.op, lse_parts=self.lp)
+        ra.lse_merge(self.op, self.lp, o=self.o_loc, lse=self.l_loc)
+        self.od, self.ld = self.cp.cp_lse_ag_out_rs(self.o_loc, self.l_loc, rescale=self.rescale)
+        if e: e[3].record()
+
+    def decode_bytes(self):
+        return Workload.decode_bytes(self)
+
+
+def run_dist(args, rank, world, dev):
+    """The benchmark line of the step split across `world` ranks (strong scaling: the same prefill
+    and decode, whatever the number of ranks)."""
+    from context_long_sequence_ring_gb300 import ringattn as ra
+    ra.lib()
+    wl = DistWorkload(ra, dev, rank, world)
+    P = PREFILL
+    for _ in range(args.warmup):
+        wl.step()
+    torch.cuda.synchronize()
+    if ra.device_status() != 0:
+        raise RuntimeError("device status after warm-up: %s" % ra.last_error())
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    _barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+        t0.record()
+        for i in range(args.steps):
+            wl.step(evs[i])
+        t1.record()
+        torch.cuda.synchronize()
+    _barrier(world)
+    ms_step = _max_over_ranks(t0.elapsed_time(t1), world, dev) / args.steps
+    if ra.device_status() != 0:
+        raise RuntimeError("device status after timing: %s" % ra.last_error())
+    ring_ms = _max_over_ranks(statistics.mean(e[0].elapsed_time(e[1]) for e in evs), world, dev)
+    dec_ms = _max_over_ranks(statistics.mean(e[2].elapsed_time(e[3]) for e in evs), world, dev)
+    flops = causal_flops(P["B"], P["Hq"], P["S"], P["d"])
+    dec_bytes, kv_bytes = wl.decode_bytes()
+    pk = _peaks()
+    # end to end, copies serial with the step: this rank's inputs in from pinned host buffers, its
+    # outputs (its rows of O and LSE, its heads of the decode output) back
+    host_in = {n: getattr(wl, n).cpu().pin_memory() for n in ("q", "k", "v", "qd", "new_k", "new_v")}
+    wl.step()
+    torch.cuda.synchronize()
+    host_out = {n: torch.empty(getattr(wl, n).shape, dtype=getattr(wl, n).dtype).pin_memory()
+                for n in ("o", "lse", "od", "ld")}
+    n_e2e = max(1, min(args.steps, 5))
+    _barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(n_e2e):
+        for n, h in host_in.items():
+            getattr(wl, n).copy_(h, non_blocking=True)
+        wl.step()
+        for n, h in host_out.items():
+            h.copy_(getattr(wl, n), non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = _max_over_ranks(e0.elapsed_time(e1), world, dev) / n_e2e
+    h2d = sum(x.numel() * x.element_size() for x in host_in.values())
+    d2h = sum(x.numel() * x.element_size() for x in host_out.values())
+    per_gpu = flops / world / (ring_ms * 1e-3) / 1e12
+    return {
+        "metric": METRIC, "value": round(flops / (ms_step * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 3), "higher_is_better": True,
+        "scaling": "strong", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded counter-based N(0,1), bf16)",
+        "config": {"workload": workload_name(), "prefill": PREFILL, "decode": dict(DECODE),
+                   "l2": "inputs larger than L2",
+                   "parallelism": "context parallel over %d ranks: prefill ring of %d zigzag ranks (K/V blocks passed "
+                                  "by NCCL send/recv), decode KV cache sharded %d devices per rank with "
+                                  "cp_lse_ag_out_rs" % (world, world, wl.n_dev)},
+        "parts": {"ring_ms": round(ring_ms, 3), "ring_tflops_per_gpu": round(per_gpu, 1),
+                  "decode_merge_ms": round(dec_ms, 4), "decode_merge_gbs": round(dec_bytes / (dec_ms * 1e-3) / 1e9, 1),
+                  "decode_kv_bytes": kv_bytes, "decode_alg_bytes": dec_bytes},
+        "roofline": {"bound": "tensor", "achieved": round(per_gpu, 1), "peak": pk["bf16"], "unit": "TFLOP/s",
+                     "frac": round(per_gpu / pk["bf16"], 4), "traffic": None,
+                     "kernel": "attn_pair_kernel<StepPolicy> (one ring step per launch, %d per rank)" % world,
+                     "peak_kind": "bf16 dense burst (%s)" % pk["src"],
+                     "algorithmic": "%.4g FLOP per rank over its %d steps, time including exposed communication"
+                                    % (flops / world, world)},
+        "e2e": {"value": round(flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3),
+                "copies": "serial with the step, this rank's shard in and its outputs out"},
+        "gpu_launches": (world + 5) * args.steps,
+        "clocks": clk.summary(),
+    }
+
+
 def run_ours(args, rank, world, dev):
     from context_long_sequence_ring_gb300 import ringattn as ra
     ra.lib()
@@ -402,6 +571,7 @@ def run_ours(args, rank, world, dev):
     line["next_rope_prologue"] = measure_rope(ra, wl)
     line["merge_stress"] = measure_merge(ra, dev)
     line["varlen_prefill"] = measure_varlen(ra, dev)
+    line["cp_ring_emulated"] = measure_ring_dist(ra, wl)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_rows)
     return line
@@ -453,6 +623,8 @@ def run_parts(args, dev):
         out["segmented"] = measure_segmented(ra, dev)
     if "varlen" in parts:
         out["varlen"] = measure_varlen(ra, dev)
+    if "ringdist" in parts:
+        out["ringdist"] = measure_ring_dist(ra, wl)
     print(json.dumps(out), flush=True)
 
 
@@ -546,6 +718,48 @@ def measure_varlen(ra, dev, reps=5):
     tf = flops / (ms * 1e-3) / 1e12
     return {"config": V, "ms": round(ms, 3), "tflops": round(tf, 1),
             "frac_of_bf16_sustained": round(tf / _peaks()["bf16_sus"], 4)}
+
+
+RING_DIST = dict(ranks=8)
+
+
+def measure_ring_dist(ra, wl, reps=3):
+    """The prefill as the ranks of a ring across devices, all emulated on this GPU: each rank holds
+    its head-tail chunk pair, every step is one ra_ring_step_fwd launch on the block the rank holds,
+    and the blocks move between the ranks' buffers by device copies on a side stream (double
+    buffering).  All ranks' steps run one after the other here, so the time is the work of the whole
+    ring on one device; on N devices each would run 1/N of it."""
+    from context_long_sequence_ring_gb300 import cp_dist
+    P = PREFILL
+    if "prefill" not in wl.parts or P["B"] != 1:
+        return None
+    N = RING_DIST["ranks"]
+    perm, _ = ra.zigzag_partition([P["S"]], N)
+    c = P["S"] // (2 * N)
+    locs = [perm[r * 2 * c:(r + 1) * 2 * c] for r in range(N)]
+    qs = [ra.gather_rows(wl.q, i) for i in locs]
+    ks = [ra.gather_rows(wl.k, i) for i in locs]
+    vs = [ra.gather_rows(wl.v, i) for i in locs]
+    steps = [ra.ring_step_fn(N, r, True) for r in range(N)]
+
+    def run():
+        return cp_dist.ring_attention_local(qs, ks, vs, step=lambda r, *a: steps[r](*a))
+    run()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        run()
+    e1.record()
+    torch.cuda.synchronize()
+    if ra.device_status() != 0:
+        raise RuntimeError("device status after the emulated ring: %s" % ra.last_error())
+    ms = e0.elapsed_time(e1) / reps
+    tf = causal_flops(1, P["Hq"], P["S"], P["d"]) / (ms * 1e-3) / 1e12
+    del qs, ks, vs
+    return {"ranks": N, "step_launches": N * N, "ms_all_ranks": round(ms, 3), "tflops": round(tf, 1),
+            "frac_of_bf16_burst": round(tf / _peaks()["bf16"], 4),
+            "note": "every rank's ring steps on one GPU, blocks rotated by device copies; not in value"}
 
 
 MERGE = dict(P=8, T=32768, H=32, d=128, seed=7)
@@ -727,11 +941,15 @@ def main():
     ap.add_argument("--parts", default="all",
                     help="'all' for the benchmark line, else a comma list of 'prefill', 'decode', 'rope' (the "
                          "RoPE prologue, needs 'prefill'), 'reorg' (the KV reorg, needs 'decode'), 'merge', "
-                         "'segmented' and 'varlen' to run only those parts (profiler captures)")
+                         "'segmented', 'varlen' and 'ringdist' (the ring across emulated devices, needs 'prefill') to run "
+                         "only those parts (profiler captures)")
     ap.add_argument("--prefill-seq", type=int, default=None, help="override S of the prefill (multiple of 2N)")
     ap.add_argument("--decode-requests", type=int, default=None, help="override the number of decode requests")
     ap.add_argument("--merge-tokens", type=int, default=None, help="override T of the stand-alone merge")
     ap.add_argument("--decode-split", type=int, default=None, help="override the decode's virtual blocks per split")
+    ap.add_argument("--cp-dist", action="store_true",
+                    help="run the step split across the job's ranks (the path used for more than one GPU) even "
+                         "on one rank")
     ap.add_argument("--prefill-shape", default=None,
                     help="B,Hq,Hkv,S,N of the prefill, for the parts runs (e.g. 1,8,8,8192,8 or 2,32,8,32768,8)")
     args = ap.parse_args()
@@ -764,12 +982,16 @@ def main():
     if args.parts != "all":
         run_parts(args, dev)
         return
-    if world > 1:
+    if world > 1 or args.cp_dist:
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        os.environ.setdefault("MASTER_PORT", "29533")
+        os.environ.setdefault("RANK", str(rank))
+        os.environ.setdefault("WORLD_SIZE", str(world))
         torch.distributed.init_process_group("nccl", device_id=dev)
-    line = run_ours(args, rank, world, dev)
+    line = run_dist(args, rank, world, dev) if (world > 1 or args.cp_dist) else run_ours(args, rank, world, dev)
     if rank == 0:
         print(json.dumps(line), flush=True)
-    if world > 1:
+    if torch.distributed.is_initialized():
         torch.distributed.destroy_process_group()
 
 

@@ -21,7 +21,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libringattn.so")
 
 SOURCES = ["ra_api.cu", "ra_cache.cu", "ra_decode.cu", "ra_attn_f32.cu", "ra_attn_bf16.cu", "ra_attn_block.cu",
-           "ra_rope.cu"]
+           "ra_rope.cu", "ra_ring_step.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", INCLUDE, "-I", CSRC]

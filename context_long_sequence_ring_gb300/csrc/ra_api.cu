@@ -46,7 +46,7 @@ extern "C" ra_status ra_device_status(ra_stream stream) {
   if (e != cudaSuccess) return ra::cuda_status(e, "cudaStreamSynchronize");
   int (*fetch[])(int*) = {ra::fetch_error_api, ra::fetch_error_cache, ra::fetch_error_decode,
                           ra::fetch_error_attn_f32, ra::fetch_error_attn_bf16, ra::fetch_error_attn_block,
-                          ra::fetch_error_rope};
+                          ra::fetch_error_rope, ra::fetch_error_ring_step};
   const char* names[] = {"partition/gather", "kv cache", "decode/merge", "attention fp32",
                          "ring attention bf16", "block attention bf16", "rope gather"};
   ra_status first = RA_OK;

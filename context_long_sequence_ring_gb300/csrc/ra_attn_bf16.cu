@@ -37,62 +37,13 @@
 // by more than 2^8 (the stale max is exact as long as l and O use the same
 // reference and P stays in range).
 #include "ra_attn_pair.cuh"
+#include "ra_ring_sched.cuh"
 
 RA_DEFINE_ERROR_FETCH(fetch_error_attn_bf16)
 
 namespace {
 
 using namespace ra::sm100;
-
-// ------------------------------------------------------------------ schedule
-struct Sched {
-  int N, c, nt, causal;  // ranks, chunk length, 128-row query tiles per chunk, causal flag
-  int bnk, ntk;          // key tile length and key tiles per chunk
-};
-
-// Iterates the K/V tiles one query tile (chunk qc, tile qi) meets, in ring
-// order: ranks s = r, r-1, ..., each rank's head chunk s, then its tail chunk
-// 2N-1-s.  Under the causal mask chunks after qc are skipped and, in qc itself,
-// only key tiles that start at or before the tile's last query are visited.
-struct KvIter {
-  int N, ntk, causal, qc, r, diag_lim;
-  int t, h, ki;
-  __device__ void init(const Sched& s, int qc_, int qi) {
-    N = s.N; ntk = s.ntk; causal = s.causal; qc = qc_;
-    r = qc < N ? qc : 2 * N - 1 - qc;
-    const int q_valid = min(BM, s.c - qi * BM);
-    diag_lim = min(ntk, (qi * BM + q_valid - 1) / s.bnk + 1);
-    t = 0; h = 0; ki = -1;
-  }
-  __device__ bool next(int& kc, int& kt) {
-    while (t < N) {
-      const int s = (r - t + N) % N;             // rank whose block is held at step t
-      const int ch = h == 0 ? s : 2 * N - 1 - s;  // its head, then its tail chunk
-      const int lim = !causal ? ntk : (ch < qc ? ntk : (ch == qc ? diag_lim : 0));
-      ++ki;
-      if (ki < lim) { kc = ch; kt = ki; return true; }
-      ki = -1;
-      if (++h == 2) { h = 0; ++t; }
-    }
-    return false;
-  }
-};
-
-__device__ __forceinline__ int n_kv_tiles(const Sched& s, int qc, int qi) {
-  if (!s.causal) return 2 * s.N * s.ntk;
-  const int q_valid = min(BM, s.c - qi * BM);
-  return qc * s.ntk + min(s.ntk, (qi * BM + q_valid - 1) / s.bnk + 1);
-}
-
-// Causal mask of key tile (kc, kt) for query row `row` of tile (qc, qi):
-// the number of leading visible columns and whether any column is masked.
-__device__ __forceinline__ void tile_mask(const Sched& s, int qc, int qi, int kc, int kt, int row, int& col_lim,
-                                          bool& masked) {
-  const int kv_valid = min(s.bnk, s.c - kt * s.bnk);
-  const bool same = s.causal && kc == qc;
-  col_lim = same ? min(kv_valid, qi * BM + row - kt * s.bnk + 1) : kv_valid;
-  masked = (same && kt * s.bnk + kv_valid - 1 > qi * BM) || kv_valid < s.bnk;
-}
 
 struct Params {
   int B, Hq, Hkv, S, N, c, nt, causal, layout, group;
@@ -407,7 +358,7 @@ __device__ __forceinline__ Item2 decode_item2(const Params& p, int idx) {
 // Ring schedule: a mirrored pair of query tiles of one virtual rank, K/V tiles
 // in ring order, causal mask by original position, bf16 output.
 template <int D>
-struct RingPolicy {
+struct RingPolicy : PolicyDefaults {
   using Args = Params;
   struct KvPos {
     KvIter it;
@@ -468,7 +419,7 @@ struct RingPolicy {
 // otherwise (small problems, to fill the SMs) one pair per CTA, the heaviest
 // pairs first.  A missing second tile (odd tile count) is an empty slot.
 template <int D>
-struct RingTilePolicy {
+struct RingTilePolicy : PolicyDefaults {
   using Args = Params;
   using KvPos = typename RingPolicy<D>::KvPos;
   const Params& p;
@@ -557,7 +508,7 @@ struct VarlenParams {
 
 // Adjacent-tile schedule (as RingTilePolicy) within one request of a varlen call.
 template <int D>
-struct RingVarlenPolicy {
+struct RingVarlenPolicy : PolicyDefaults {
   using Args = VarlenParams;
   using KvPos = typename RingPolicy<D>::KvPos;
   const VarlenParams& p;

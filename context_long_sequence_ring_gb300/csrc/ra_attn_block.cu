@@ -65,7 +65,7 @@ __device__ __forceinline__ void block_mask(const BlockParams& p, int qt, int kt,
 // tile and a head pair per CTA, key tiles 0..n-1 of the block in order, fp32
 // partial output.
 template <int D>
-struct BlockPolicy {
+struct BlockPolicy : PolicyDefaults {
   using Args = BlockParams;
   struct KvPos {
     int kt;
@@ -123,7 +123,7 @@ struct BlockPolicy {
 // (under the causal mask a superset of the earlier tile's).  A slot past the
 // last query tile is empty.
 template <int D>
-struct BlockTilePolicy {
+struct BlockTilePolicy : PolicyDefaults {
   using Args = BlockParams;
   using KvPos = typename BlockPolicy<D>::KvPos;
   const BlockParams& p;

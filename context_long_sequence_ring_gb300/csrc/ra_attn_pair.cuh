@@ -14,7 +14,12 @@
 //   void store_o(int h, int row, int col0, const uint32_t (&o)[32], float inv_l)
 //   void store_lse(int h, int row, float lse)
 //   void write_empty(int tid, int nthreads)   outputs of a CTA with no query tile to run (tiles() == 0)
-// and Args carries scale_log2 and wait_limit.
+//   void skipped_rows(int h, int row)    outputs of slot h, row `row` of the CTA's query tiles that
+//                                        tiles() leaves out (called once per softmax thread first)
+//   void prepare_row(int h, int row, float lse2, float inv_l)
+//                                        called before the store_o calls of a stored row, with the
+//                                        row's log2-sum-exp (-inf if it saw no key)
+// and Args carries scale_log2 and wait_limit.  PolicyDefaults gives the last two as no-ops.
 #pragma once
 
 #include "ra_attn_tc.cuh"
@@ -44,6 +49,12 @@ using namespace ra::sm100;
 // overwrite the columns PV_h(j) reads.  A softmax warpgroup only waits for
 // the previous P.V when it must rescale O (lazy rescale, threshold 2^8).
 // ===========================================================================
+// No-op defaults of the two optional policy hooks.
+struct PolicyDefaults {
+  __device__ void skipped_rows(int, int) const {}
+  __device__ void prepare_row(int, int, float, float) {}
+};
+
 template <int D>
 struct __align__(1024) Smem2 {
   uint8_t q[2][BM * D * 2];
@@ -239,6 +250,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
     const uint32_t colS = h * BN, colO = kColO + h * D;
     uint32_t s_cnt = 0, pv_base = 0;
     bool ok = true;
+    pol.skipped_rows(h, row);
     for (int ti = 0; ti < n_tiles && ok; ++ti) {
       pol.set_tile(ti);
       const int q_valid = pol.q_valid(h);
@@ -284,6 +296,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
       tc_fence_after();
       const float inv_l = l > 0.f ? 1.f / l : 0.f;
       const bool row_ok = row < q_valid;
+      if (row_ok) pol.prepare_row(h, row, l > 0.f ? m + log2f(l) : -CUDART_INF_F, inv_l);
 #pragma unroll
       for (int c4 = 0; c4 < D / 32; ++c4) {
         uint32_t orr[32];

@@ -29,6 +29,7 @@ int fetch_error_attn_f32(int* where);
 int fetch_error_attn_bf16(int* where);
 int fetch_error_attn_block(int* where);
 int fetch_error_rope(int* where);
+int fetch_error_ring_step(int* where);
 
 }  // namespace ra
 

@@ -64,6 +64,7 @@ struct DecodeParams {
   float* o_parts;              // [P, R, Hq, D]
   float* lse_parts;            // [P, R, Hq]
   int R, Hq, Hkv, G, bs, interleave, W, max_vb, split_blocks, n_splits;
+  int dev0;                    // the cache holds devices dev0, dev0+1, ... (blockIdx.y counts from dev0)
   long long num_blocks;
   float scale_log2;
 };
@@ -86,7 +87,8 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
   constexpr int KS = D / 16;  // k-steps of the Q.K^T product
   __shared__ __align__(16) uint16_t p_smem[kWarps][8][16];  // P^T [head][slot] bf16 per warp
 
-  const int sp = blockIdx.x, w = blockIdx.y, r = blockIdx.z;
+  const int sp = blockIdx.x, wl = blockIdx.y, r = blockIdx.z;
+  const int w = p.dev0 + wl;  // the device's number among all W (token ownership)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
   const int L = p.ctx[r];
@@ -94,8 +96,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
   const int nvb = static_cast<int>((L + Vsz - 1) / Vsz);
   const int vb0 = sp * p.split_blocks;
   const int vb1 = min(nvb, vb0 + p.split_blocks);
-  const int P = p.W * p.n_splits;
-  const int part = w * p.n_splits + sp;
+  const int part = wl * p.n_splits + sp;
 
   for (int kvh = warp; kvh < p.Hkv; kvh += kWarps) {
     // ---- Q fragments (bf16 pairs), heads >= G are zero
@@ -122,7 +123,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
         continue;
       }
       const int64_t head_base =
-          ((static_cast<int64_t>(w) * p.num_blocks + blk) * p.Hkv + kvh) * p.bs * D;
+          ((static_cast<int64_t>(wl) * p.num_blocks + blk) * p.Hkv + kvh) * p.bs * D;
       const __nv_bfloat16* kb = p.kc + head_base;
       const __nv_bfloat16* vbp = p.vc + head_base;
       const bool block_full = static_cast<int64_t>(vb + 1) * Vsz <= L;
@@ -264,7 +265,6 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
       }
     }
   }
-  (void)P;
 }
 
 // One warp per (token, head) row: LSE = M + ln sum_p e^{LSE_p - M},
@@ -397,6 +397,79 @@ extern "C" ra_status ra_cp_decode_workspace_size(int32_t R, int32_t Hq, int32_t 
   return RA_OK;
 }
 
+namespace {
+// Checks shared by the decode entry points; fills the kernel parameters.
+ra_status decode_params(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
+                        const int32_t* ctx_lens, int32_t R, int32_t Hq, int32_t Hkv, int32_t d, int32_t block_size,
+                        int32_t interleave, int32_t pcp, int32_t dcp, int32_t dev0, int32_t n_dev,
+                        int32_t max_vblocks, int64_t num_blocks, float scale, int32_t split_blocks,
+                        DecodeParams& prm) {
+  RA_REQUIRE(R >= 1 && Hq >= 1 && Hkv >= 1 && block_size >= 1 && interleave >= 1 && pcp >= 1 &&
+                 dcp >= 1 && max_vblocks >= 1 && num_blocks >= 1 && split_blocks >= 1,
+             "sizes must be >= 1");
+  RA_REQUIRE(block_size % interleave == 0,
+             "block_size %% cp_kv_cache_interleave_size must be 0 (block_size=%d, interleave=%d)",
+             block_size, interleave);
+  RA_REQUIRE(Hq % Hkv == 0, "Hq (%d) must be a multiple of Hkv (%d)", Hq, Hkv);
+  const int W = pcp * dcp;
+  RA_REQUIRE(dev0 >= 0 && n_dev >= 1 && dev0 + n_dev <= W, "devices [%d, %d) must lie in [0, pcp*dcp = %d)", dev0,
+             dev0 + n_dev, W);
+  if (d != 64 && d != 128) return ra::fail(RA_ERR_UNSUPPORTED, "head dim %d not supported (64 or 128)", d);
+  if (Hq / Hkv > 8) return ra::fail(RA_ERR_UNSUPPORTED, "GQA group %d > 8 not supported", Hq / Hkv);
+  if (block_size % 16 != 0) return ra::fail(RA_ERR_UNSUPPORTED, "block_size must be a multiple of 16");
+  RA_REQUIRE(q && k_cache && v_cache && block_table && ctx_lens, "NULL pointer");
+  RA_REQUIRE(ra::aligned16(q) && ra::aligned16(k_cache) && ra::aligned16(v_cache),
+             "q and the caches must be 16-byte aligned");
+  const int n_splits = n_splits_of(max_vblocks, split_blocks);
+  RA_REQUIRE(n_splits <= 65535 && n_dev <= 65535 && R <= 65535, "grid too large");
+  prm.q = static_cast<const __nv_bfloat16*>(q);
+  prm.kc = static_cast<const __nv_bfloat16*>(k_cache);
+  prm.vc = static_cast<const __nv_bfloat16*>(v_cache);
+  prm.block_table = block_table;
+  prm.ctx = ctx_lens;
+  prm.R = R; prm.Hq = Hq; prm.Hkv = Hkv; prm.G = Hq / Hkv; prm.bs = block_size;
+  prm.interleave = interleave; prm.W = W; prm.max_vb = max_vblocks;
+  prm.split_blocks = split_blocks; prm.n_splits = n_splits; prm.num_blocks = num_blocks;
+  prm.dev0 = dev0;
+  prm.scale_log2 = (scale > 0.f ? scale : 1.f / sqrtf(static_cast<float>(d))) * kLog2e;
+  return RA_OK;
+}
+
+ra_status launch_decode(const DecodeParams& prm, int n_dev, int d, cudaStream_t stream) {
+  dim3 grid(prm.n_splits, n_dev, prm.R);
+  if (d == 128)
+    cp_decode_kernel<128><<<grid, kWarps * 32, 0, stream>>>(prm);
+  else
+    cp_decode_kernel<64><<<grid, kWarps * 32, 0, stream>>>(prm);
+  RA_LAUNCH_CHECK("cp_decode_kernel");
+  return RA_OK;
+}
+}  // namespace
+
+extern "C" ra_status ra_cp_decode_partials(const void* q, const void* k_cache, const void* v_cache,
+                                           const int32_t* block_table, const int32_t* ctx_lens, int32_t R,
+                                           int32_t Hq, int32_t Hkv, int32_t d, int32_t block_size,
+                                           int32_t interleave, int32_t pcp, int32_t dcp, int32_t dev0,
+                                           int32_t n_dev, int32_t max_vblocks, int64_t num_blocks, float scale,
+                                           int32_t split_blocks, float* o_parts, float* lse_parts,
+                                           int32_t* n_parts_out, ra_stream stream) {
+  ra::clear_error();
+  DecodeParams prm;
+  ra_status st = decode_params(q, k_cache, v_cache, block_table, ctx_lens, R, Hq, Hkv, d, block_size, interleave,
+                               pcp, dcp, dev0, n_dev, max_vblocks, num_blocks, scale, split_blocks, prm);
+  if (st != RA_OK) return st;
+  const int64_t P = static_cast<int64_t>(n_dev) * prm.n_splits;
+  RA_REQUIRE(P < (int64_t(1) << 31), "too many partials");
+  if (n_parts_out) *n_parts_out = static_cast<int32_t>(P);
+  if (o_parts == nullptr && lse_parts == nullptr) return RA_OK;  // size query
+  RA_REQUIRE(o_parts && lse_parts, "o_parts and lse_parts are given together");
+  RA_REQUIRE(ra::aligned16(o_parts) && reinterpret_cast<uintptr_t>(lse_parts) % 4 == 0,
+             "o_parts must be 16-byte aligned, lse_parts 4-byte aligned");
+  prm.o_parts = o_parts;
+  prm.lse_parts = lse_parts;
+  return launch_decode(prm, n_dev, d, stream);
+}
+
 extern "C" ra_status ra_cp_decode(const void* q, const void* k_cache, const void* v_cache,
                                   const int32_t* block_table, const int32_t* ctx_lens, int32_t R,
                                   int32_t Hq, int32_t Hkv, int32_t d, int32_t block_size,
@@ -405,50 +478,91 @@ extern "C" ra_status ra_cp_decode(const void* q, const void* k_cache, const void
                                   ra_dtype out_dt, float* lse, void* workspace, size_t ws_bytes,
                                   ra_stream stream) {
   ra::clear_error();
-  RA_REQUIRE(R >= 1 && Hq >= 1 && Hkv >= 1 && block_size >= 1 && interleave >= 1 && pcp >= 1 &&
-                 dcp >= 1 && max_vblocks >= 1 && num_blocks >= 1 && split_blocks >= 1,
-             "sizes must be >= 1");
-  RA_REQUIRE(block_size % interleave == 0,
-             "block_size %% cp_kv_cache_interleave_size must be 0 (block_size=%d, interleave=%d)",
-             block_size, interleave);
-  RA_REQUIRE(Hq % Hkv == 0, "Hq (%d) must be a multiple of Hkv (%d)", Hq, Hkv);
   RA_REQUIRE(out_dt == RA_F32 || out_dt == RA_BF16, "unknown out dtype");
-  if (d != 64 && d != 128) return ra::fail(RA_ERR_UNSUPPORTED, "head dim %d not supported (64 or 128)", d);
-  if (Hq / Hkv > 8) return ra::fail(RA_ERR_UNSUPPORTED, "GQA group %d > 8 not supported", Hq / Hkv);
-  if (block_size % 16 != 0) return ra::fail(RA_ERR_UNSUPPORTED, "block_size must be a multiple of 16");
-  RA_REQUIRE(q && k_cache && v_cache && block_table && ctx_lens && o && workspace, "NULL pointer");
-  RA_REQUIRE(ra::aligned16(q) && ra::aligned16(k_cache) && ra::aligned16(v_cache) && ra::aligned16(o) &&
-                 ra::aligned16(workspace),
-             "q, caches, o and workspace must be 16-byte aligned");
-  size_t need = 0;
-  ra_status st = ra_cp_decode_workspace_size(R, Hq, d, max_vblocks, pcp, dcp, split_blocks, &need);
-  if (st != RA_OK) return st;
-  RA_REQUIRE(ws_bytes >= need, "workspace too small (%zu < %zu bytes)", ws_bytes, need);
-  const int W = pcp * dcp;
-  const int n_splits = n_splits_of(max_vblocks, split_blocks);
-  RA_REQUIRE(n_splits <= 65535 && W <= 65535 && R <= 65535, "grid too large");
-  const int64_t P = static_cast<int64_t>(W) * n_splits;
   DecodeParams prm;
-  prm.q = static_cast<const __nv_bfloat16*>(q);
-  prm.kc = static_cast<const __nv_bfloat16*>(k_cache);
-  prm.vc = static_cast<const __nv_bfloat16*>(v_cache);
-  prm.block_table = block_table;
-  prm.ctx = ctx_lens;
+  ra_status st = decode_params(q, k_cache, v_cache, block_table, ctx_lens, R, Hq, Hkv, d, block_size, interleave,
+                               pcp, dcp, 0, pcp * dcp, max_vblocks, num_blocks, scale, split_blocks, prm);
+  if (st != RA_OK) return st;
+  RA_REQUIRE(o && workspace, "NULL pointer");
+  RA_REQUIRE(ra::aligned16(o) && ra::aligned16(workspace), "o and workspace must be 16-byte aligned");
+  size_t need = 0;
+  if ((st = ra_cp_decode_workspace_size(R, Hq, d, max_vblocks, pcp, dcp, split_blocks, &need)) != RA_OK) return st;
+  RA_REQUIRE(ws_bytes >= need, "workspace too small (%zu < %zu bytes)", ws_bytes, need);
+  const int64_t P = static_cast<int64_t>(prm.W) * prm.n_splits;
   prm.o_parts = static_cast<float*>(workspace);
   prm.lse_parts = reinterpret_cast<float*>(static_cast<char*>(workspace) +
                                            ra::ceil_div(P * R * Hq * d * 4, 256) * 256);
-  prm.R = R; prm.Hq = Hq; prm.Hkv = Hkv; prm.G = Hq / Hkv; prm.bs = block_size;
-  prm.interleave = interleave; prm.W = W; prm.max_vb = max_vblocks;
-  prm.split_blocks = split_blocks; prm.n_splits = n_splits; prm.num_blocks = num_blocks;
-  prm.scale_log2 = (scale > 0.f ? scale : 1.f / sqrtf(static_cast<float>(d))) * kLog2e;
-  dim3 grid(n_splits, W, R);
-  if (d == 128)
-    cp_decode_kernel<128><<<grid, kWarps * 32, 0, stream>>>(prm);
-  else
-    cp_decode_kernel<64><<<grid, kWarps * 32, 0, stream>>>(prm);
-  RA_LAUNCH_CHECK("cp_decode_kernel");
+  if ((st = launch_decode(prm, prm.W, d, stream)) != RA_OK) return st;
   return launch_merge(prm.o_parts, prm.lse_parts, static_cast<int>(P), static_cast<int64_t>(R) * Hq, d, o,
                       out_dt, lse, stream);
+}
+
+// ===========================================================================
+// Step 2 of cp_lse_ag_out_rs (vLLM-Ascend "Context Parallel (CP)", DCP
+// decode): with every device's LSE gathered, device w scales its own partial
+// O_w by e^{LSE_w - LSE}, LSE = ln sum_v e^{LSE_v}, and lays it out by the
+// device that keeps each head after the reduce-scatter.  One warp per
+// (request, head) row.
+// ===========================================================================
+namespace {
+__global__ void lse_rescale_kernel(const float* __restrict__ o_local, const float* __restrict__ lse_all, int W,
+                                   int w, int64_t R, int Hq, int d, float* __restrict__ o_scaled,
+                                   float* __restrict__ lse_total) {
+  const int lane = threadIdx.x & 31;
+  const int64_t rows = R * Hq;
+  const int hs = Hq / W;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t row = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; row < rows;
+       row += nwarps) {
+    const int64_t r = row / Hq;
+    const int h = static_cast<int>(row % Hq);
+    float M = -CUDART_INF_F;
+    for (int v = lane; v < W; v += 32) M = fmaxf(M, lse_all[static_cast<int64_t>(v) * rows + row]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float tot = 0.f;
+    if (M != -CUDART_INF_F)
+      for (int v = lane; v < W; v += 32) {
+        const float x = lse_all[static_cast<int64_t>(v) * rows + row];
+        tot += x == -CUDART_INF_F ? 0.f : expf(x - M);
+      }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+    const float lse = M == -CUDART_INF_F ? -CUDART_INF_F : M + logf(tot);
+    const float mine = lse_all[static_cast<int64_t>(w) * rows + row];
+    const float wgt = (mine == -CUDART_INF_F || lse == -CUDART_INF_F) ? 0.f : expf(mine - lse);
+    const int v = h / hs, j = h % hs;
+    float* dst = o_scaled + ((static_cast<int64_t>(v) * R + r) * hs + j) * d;
+    const float* src = o_local + row * d;
+    for (int e = 4 * lane; e < d; e += 128) {
+      float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (wgt != 0.f) {   // a partial with no key is not read
+        a = *reinterpret_cast<const float4*>(src + e);
+        a.x *= wgt; a.y *= wgt; a.z *= wgt; a.w *= wgt;
+      }
+      *reinterpret_cast<float4*>(dst + e) = a;
+    }
+    if (lse_total && v == w && lane == 0) lse_total[r * hs + j] = lse;
+  }
+}
+}  // namespace
+
+extern "C" ra_status ra_cp_lse_rescale(const float* o_local, const float* lse_all, int32_t W, int32_t w, int64_t R,
+                                       int32_t Hq, int32_t d, float* o_scaled, float* lse_total,
+                                       ra_stream stream) {
+  ra::clear_error();
+  RA_REQUIRE(W >= 1 && w >= 0 && w < W, "w (%d) must be in [0, W = %d)", w, W);
+  RA_REQUIRE(R >= 0 && Hq >= 1 && d >= 1, "R >= 0, Hq and d >= 1");
+  RA_REQUIRE(Hq % W == 0, "Hq (%d) must be a multiple of W (%d)", Hq, W);
+  if (d % 4 != 0) return ra::fail(RA_ERR_UNSUPPORTED, "d must be a multiple of 4 (got %d)", d);
+  if (R == 0) return RA_OK;
+  RA_REQUIRE(o_local && lse_all && o_scaled, "NULL pointer");
+  RA_REQUIRE(ra::aligned16(o_local) && ra::aligned16(o_scaled), "o_local and o_scaled must be 16-byte aligned");
+  const int64_t blocks = std::min<int64_t>(ra::ceil_div(R * Hq * 32, 256), 152 * 16);
+  lse_rescale_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(o_local, lse_all, W, w, R, Hq, d, o_scaled,
+                                                                         lse_total);
+  RA_LAUNCH_CHECK("lse_rescale_kernel");
+  return RA_OK;
 }
 
 // ===========================================================================

@@ -38,6 +38,8 @@ SIGNATURES = {
     "ra_ring_schedule_counts": [_i32, _i32, _i32, _vp, _vp],
     "ra_ring_schedule_counts_ex": [_i32, _i32, _i32, _i32, _vp, _vp],
     "ra_lse_merge": [_vp, _vp, _i32, _i64, _i32, _i32, _vp, _c.c_int, _vp, _vp],
+    "ra_ring_step_fwd": [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _vp, _vp, _vp,
+                         _c.c_int, _vp, _vp],
     "ra_attn_block_fwd": [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i64, _i64, _i32, _f32, _vp, _vp, _vp],
     "ra_segmented_prefill_workspace_size": [_i32, _i32, _i32, _i32, _i32, _c.POINTER(_sz)],
     "ra_segmented_prefill_fwd": [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i64, _i32, _f32, _i32, _vp,
@@ -51,6 +53,9 @@ SIGNATURES = {
                      _i32, _vp, _c.c_int, _vp, _vp, _sz, _vp],
     "ra_cp_decode_noalloc": [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i64,
                              _f32, _i32, _vp, _c.c_int, _vp, _vp],
+    "ra_cp_decode_partials": [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
+                              _i32, _i64, _f32, _i32, _vp, _vp, _c.POINTER(_i32), _vp],
+    "ra_cp_lse_rescale": [_vp, _vp, _i32, _i32, _i64, _i32, _i32, _vp, _vp, _vp],
     "ra_selftest_wait_timeout": [_i64, _vp],
     "ra_synth_fill": [_u64, _i64, _vp, _i32, _vp, _vp],
 }
@@ -229,6 +234,34 @@ def ring_attn_fwd_varlen(q, k, v, seq_lens: Sequence[int], causal: bool, n_ranks
     return o, lse
 
 
+def ring_step_fwd(q, k, v, n_ranks: int, rank: int, src: int, causal: bool, o_in=None, lse_in=None,
+                  o_out=None, lse_out=None, B: int = 1, scale: Optional[float] = None):
+    """One ring step of rank ``rank``: its local queries q [B*2c, Hq, d] (chunks rank and 2N-1-rank
+    of each sequence) against the held block k/v [B*2c, Hkv, d] of rank ``src``, folded into the
+    running result (o_in fp32 [B*2c, Hq, d], lse_in [B*2c, Hq]; None at the first step).  o_out
+    (fp32 or bf16; may be o_in when fp32) and lse_out (may be lse_in) receive the result; fp32
+    buffers are made when they are not given.  Returns (o_out, lse_out)."""
+    _need_cuda(q, k, v, o_in, lse_in, o_out, lse_out)
+    rows, Hq, d = q.shape
+    if rows % (2 * B) != 0 or k.shape[0] != rows or v.shape[0] != rows:
+        raise ValueError("q, k, v must hold B sequences of 2c local rows each")
+    if o_out is None:
+        o_out = torch.empty((rows, Hq, d), dtype=torch.float32, device=q.device)
+    if lse_out is None:
+        lse_out = torch.empty((rows, Hq), dtype=torch.float32, device=q.device)
+    _check(lib().ra_ring_step_fwd(_ptr(q), _ptr(k), _ptr(v), B, Hq, k.shape[1], rows // (2 * B), d, n_ranks, rank,
+                                  src, 1 if causal else 0, float(scale or 0.0), _ptr(o_in), _ptr(lse_in),
+                                  _ptr(o_out), _dt(o_out), _ptr(lse_out), _stream()))
+    return o_out, lse_out
+
+
+def ring_step_fn(n_ranks: int, rank: int, causal: bool, B: int = 1, scale: Optional[float] = None):
+    """The step callable of ``cp_dist.ring_attention`` for rank ``rank``, on ra_ring_step_fwd."""
+    def step(q, k, v, src, o_in, lse_in, o_out, lse_out):
+        ring_step_fwd(q, k, v, n_ranks, rank, src, causal, o_in, lse_in, o_out, lse_out, B=B, scale=scale)
+    return step
+
+
 def attn_block_fwd(q, k, v, q_pos0: int, k_pos0: int, causal: bool, scale: Optional[float] = None,
                    o_part=None, lse_part=None):
     """Partial attention of q [Tq, Hq, d] (positions q_pos0..) over k/v [Tk, Hkv, d] (positions k_pos0..)
@@ -368,6 +401,50 @@ def cp_decode_noalloc(q, k_cache, v_cache, block_table, ctx_lens, interleave: in
                                       float(scale or 0.0), split_blocks, _ptr(o),
                                       RA_BF16 if o.dtype == torch.bfloat16 else RA_F32, _ptr(lse), _stream()))
     return o, lse
+
+
+def cp_decode_partials(q, k_cache, v_cache, block_table, ctx_lens, interleave: int, pcp: int, dcp: int,
+                       dev0: int = 0, split_blocks: int = 8, scale: Optional[float] = None, o_parts=None,
+                       lse_parts=None):
+    """Split-KV partials of the devices whose shards k_cache/v_cache [n_dev, NB, Hkv, bs, d] hold
+    (devices dev0 .. dev0+n_dev-1 of pcp*dcp) -> (O_parts fp32 [P, R, Hq, d], LSE_parts [P, R, Hq]),
+    partial p = (w - dev0) * n_splits + s.  A partial with LSE -inf has no token and unwritten O."""
+    _need_cuda(q, k_cache, v_cache, block_table, ctx_lens, o_parts, lse_parts)
+    R, Hq, d = q.shape
+    n_dev, NB, Hkv, bs, _ = k_cache.shape
+    max_vb = block_table.shape[1]
+    P = _i32(0)
+    args = (_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(ctx_lens), R, Hq, Hkv, d, bs, interleave,
+            pcp, dcp, dev0, n_dev, max_vb, NB, float(scale or 0.0), split_blocks)
+    _check(lib().ra_cp_decode_partials(*args, None, None, _c.byref(P), _stream()))
+    if o_parts is None:
+        o_parts = torch.empty((P.value, R, Hq, d), dtype=torch.float32, device=q.device)
+    if lse_parts is None:
+        lse_parts = torch.empty((P.value, R, Hq), dtype=torch.float32, device=q.device)
+    _check(lib().ra_cp_decode_partials(*args, _ptr(o_parts), _ptr(lse_parts), None, _stream()))
+    return o_parts, lse_parts
+
+
+def cp_lse_rescale(o_local, lse_all, w: int, o_scaled=None, lse_total=None):
+    """Step 2 of cp_lse_ag_out_rs on device w: o_local fp32 [R, Hq, d], lse_all [W, R, Hq] ->
+    (o_scaled [W, R, Hq/W, d], lse_total [R, Hq/W])."""
+    _need_cuda(o_local, lse_all, o_scaled, lse_total)
+    R, Hq, d = o_local.shape
+    W = lse_all.shape[0]
+    if o_scaled is None:
+        o_scaled = torch.empty((W, R, Hq // W, d), dtype=torch.float32, device=o_local.device)
+    if lse_total is None:
+        lse_total = torch.empty((R, Hq // W), dtype=torch.float32, device=o_local.device)
+    _check(lib().ra_cp_lse_rescale(_ptr(o_local), _ptr(lse_all), W, w, R, Hq, d, _ptr(o_scaled), _ptr(lse_total),
+                                   _stream()))
+    return o_scaled, lse_total
+
+
+def cp_lse_rescale_fn():
+    """The rescale callable of ``cp_dist.cp_lse_ag_out_rs``, on ra_cp_lse_rescale."""
+    def rescale(o_local, lse_all, w, o_scaled, lse_total):
+        cp_lse_rescale(o_local, lse_all, w, o_scaled, lse_total)
+    return rescale
 
 
 # ---------------------------------------------------------------------- misc

@@ -242,6 +242,50 @@ ra_status ra_attn_block_fwd(const void* q, const void* k, const void* v, int32_t
                             ra_stream stream);
 
 /* ------------------------------------------------------------------------
+ * ra_ring_step_fwd -- one step of a ring across devices, on the rank that runs
+ * it: its queries against the K/V block it holds at this step, folded into its
+ * running result.  Sources: "Parallelism-CP" diagram (each card computes its
+ * own Q against the K/V blocks that rotate around the ring); guijiagi.com
+ * "Ring Attention" tag page (ring topology: at step t rank i holds the block
+ * of rank (i - t) mod N; blockwise decomposition, a partial over some keys is
+ * carried by its log-sum-exp); vLLM-Ascend "Context Parallel (CP)" head-tail
+ * partition (rank r holds chunks r and 2N-1-r).
+ *
+ * Local layout (what the head-tail partition gives a rank): per sequence
+ * (B of them), the rank's first chunk then its second, c rows each; the row of
+ * (sequence b, half h, offset o) is (b*2 + h)*c + o.
+ * q          device bf16 [B*2c, Hq, d]: rank `rank`'s queries (chunks rank and
+ *            2N-1-rank of each sequence).
+ * k, v       device bf16 [B*2c, Hkv, d]: the block held, i.e. rank `src`'s
+ *            local K/V (chunks src and 2N-1-src).
+ * o_in, lse_in  device fp32 [B*2c, Hq, d] and [B*2c, Hq]: the running result
+ *            (normalised O and its LSE) of the steps so far, or both NULL at
+ *            the rank's first step.
+ * o_out      device [B*2c, Hq, d] out in out_dt; lse_out device fp32
+ *            [B*2c, Hq] out.  o_out may be o_in when out_dt is RA_F32 and
+ *            lse_out may be lse_in (the running result updated in place); a
+ *            bf16 o_out is the final output, given at the last step.
+ * Result: the merge of the running result with this block's partial,
+ * LSE = ln(e^{LSE_in} + e^{LSE_p}), O = e^{LSE_in - LSE} O_in + e^{LSE_p - LSE} O_p,
+ * where (O_p, LSE_p) is attention over the keys of the block visible to each
+ * query (causal != 0: original key position <= query position).  Rows that
+ * see no key of the block keep the running result (O 0, LSE -inf without one).
+ * Over the N steps (src = (rank - t) mod N, or any order) the result is the
+ * rank's rows of full attention.  Query head h reads K/V head h / (Hq/Hkv);
+ * scale <= 0 means 1/sqrt(d).  Even Hq/Hkv runs two heads per CTA, odd runs two
+ * adjacent query tiles of one head per CTA.
+ * Errors: B, Hq, Hkv, c < 1; Hq % Hkv != 0; rank or src outside [0, n_ranks);
+ * o_in without lse_in or the reverse; a bf16 o_out equal to o_in; pointers
+ * not 16-byte aligned (lse 4-byte); B*2c >= 2^31 -> RA_ERR_INVALID_ARG;
+ * d not in {64, 128} -> RA_ERR_UNSUPPORTED.
+ * ---------------------------------------------------------------------- */
+ra_status ra_ring_step_fwd(const void* q, const void* k, const void* v, int32_t B, int32_t Hq,
+                           int32_t Hkv, int32_t c, int32_t d, int32_t n_ranks, int32_t rank,
+                           int32_t src, int32_t causal, float scale, const float* o_in,
+                           const float* lse_in, void* o_out, ra_dtype out_dt, float* lse_out,
+                           ra_stream stream);
+
+/* ------------------------------------------------------------------------
  * ra_segmented_prefill_fwd -- chunked prefill with a bounded KV segment per
  * round (vLLM-Ascend "Context Parallel (CP)", chunked prefill, segmented
  * AllGatherKV): the key range [0, Tk) is cut into segments of seg_tokens; each
@@ -372,6 +416,62 @@ ra_status ra_cp_decode(const void* q, const void* k_cache, const void* v_cache,
                        int64_t num_blocks, float scale, int32_t split_blocks, void* o,
                        ra_dtype out_dt, float* lse, void* workspace, size_t ws_bytes,
                        ra_stream stream);
+
+/* ------------------------------------------------------------------------
+ * ra_cp_decode_partials -- the split-KV partials of the devices whose cache
+ * shards the caller holds, unmerged: what one device computes before the
+ * cp_lse_ag_out_rs merge across devices.  Source: vLLM-Ascend "Context
+ * Parallel (CP)", DCP decode (each device attends over its local KV shard and
+ * returns its output with its LSE) and section "Block table" (which device
+ * stores which token).
+ *
+ * q, block_table, ctx_lens, sizes, scale, split_blocks: as ra_cp_decode.
+ * dev0, n_dev  the cache holds devices dev0 .. dev0+n_dev-1 of W = pcp*dcp
+ *             (all of them: dev0 = 0, n_dev = W; one device w: dev0 = w,
+ *             n_dev = 1).
+ * k_cache, v_cache device bf16 [n_dev, num_blocks, Hkv, block_size, d]:
+ *             their shards, in that order.
+ * o_parts     device float [P, R, Hq, d] out, lse_parts device float [P, R, Hq]
+ *             out, P = n_dev * n_splits: partial p = (w - dev0)*n_splits + s
+ *             covers device w's tokens of virtual blocks [s*split_blocks,
+ *             (s+1)*split_blocks), O normalised by its own sum.  A partial
+ *             with no token has LSE -inf and its O is not written.
+ * n_parts_out host int32 out (may be NULL): P.  With o_parts and lse_parts
+ *             both NULL only P is returned and nothing is launched.
+ * Errors: as ra_cp_decode; [dev0, dev0+n_dev) outside [0, W) is
+ * RA_ERR_INVALID_ARG.
+ * ---------------------------------------------------------------------- */
+ra_status ra_cp_decode_partials(const void* q, const void* k_cache, const void* v_cache,
+                                const int32_t* block_table, const int32_t* ctx_lens, int32_t R,
+                                int32_t Hq, int32_t Hkv, int32_t d, int32_t block_size,
+                                int32_t interleave, int32_t pcp, int32_t dcp, int32_t dev0,
+                                int32_t n_dev, int32_t max_vblocks, int64_t num_blocks, float scale,
+                                int32_t split_blocks, float* o_parts, float* lse_parts,
+                                int32_t* n_parts_out, ra_stream stream);
+
+/* ------------------------------------------------------------------------
+ * ra_cp_lse_rescale -- step 2 of cp_lse_ag_out_rs on device w of W: after the
+ * all-gather of every device's LSE, scale this device's output by its merge
+ * weight and lay it out for the reduce-scatter over heads.  Source:
+ * vLLM-Ascend "Context Parallel (CP)", DCP decode (cp_lse_ag_out_rs:
+ * all-gather of the LSEs, local update of the output, reduce-scatter); the
+ * weights e^{LSE_w - LSE} of the blockwise decomposition ("Ring Attention" tag
+ * page).  Steps 1 and 3 are collectives of the caller's communication library.
+ *
+ * o_local   device float [R, Hq, d]: device w's output over its own keys
+ *           (normalised; e.g. ra_lse_merge of its ra_cp_decode_partials).
+ * lse_all   device float [W, R, Hq]: every device's LSE, device w's at w.
+ * o_scaled  device float [W, R, Hq/W, d] out: slot v holds heads
+ *           [v*Hq/W, (v+1)*Hq/W) of e^{LSE_w - LSE} O_w, LSE = ln sum_v e^{LSE_v}
+ *           (0 where LSE_w or LSE is -inf; o_local is not read there).  Summed
+ *           over devices, slot v is device v's merged output.
+ * lse_total device float [R, Hq/W] out (may be NULL): LSE of this device's
+ *           heads [w*Hq/W, (w+1)*Hq/W).
+ * Requires 0 <= w < W, Hq % W == 0, d % 4 == 0 (RA_ERR_UNSUPPORTED otherwise),
+ * o_local and o_scaled 16-byte aligned.
+ * ---------------------------------------------------------------------- */
+ra_status ra_cp_lse_rescale(const float* o_local, const float* lse_all, int32_t W, int32_t w, int64_t R,
+                            int32_t Hq, int32_t d, float* o_scaled, float* lse_total, ra_stream stream);
 
 /* ------------------------------------------------------------------------
  * ra_cp_decode_noalloc -- ra_cp_decode for callers that cannot allocate

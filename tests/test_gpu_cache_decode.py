@@ -173,8 +173,9 @@ def test_decode_matches_oracle(ra, R, lo, hi, bs, I_, pcp, dcp, Hq, Hkv, d, spli
     W = pcp * dcp
     kc_np = np.zeros((W, wl["num_blocks"], Hkv, bs, d))
     vc_np = np.zeros_like(kc_np)
-    oracle.cp_kv_scatter(kt.double().numpy(), vt.double().numpy(), slot.cpu().numpy().astype(np.int64),
-                         kc_np, vc_np, bs)
+    pos = np.concatenate([np.arange(int(L)) for L in wl["ctx_lens"]])
+    oslot = oracle.cp_slot_mapping(qsl.numpy(), pos, wl["block_table"].numpy(), bs, I_, pcp, dcp)
+    oracle.cp_kv_scatter(kt.double().numpy(), vt.double().numpy(), oslot, kc_np, vc_np, bs)
     O2, L2 = oracle.cp_decode(qd, kc_np, vc_np, wl["block_table"].numpy(), wl["ctx_lens"].numpy(), bs, I_,
                               pcp, dcp, split)
     assert_parity(o, O2, lse, L2, torch.bfloat16, "decode vs sharded oracle")
