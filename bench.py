@@ -223,7 +223,8 @@ class Workload:
         ra.gather_rows(self.v, self.perm, self.vz)
         if e: e[1].record()
         # a3-a5: ring-order attention over the N virtual ranks
-        ra.ring_attn_fwd(self.qz, self.kz, self.vz, True, P["N"], B=P["B"], layout="zigzag", o=self.oz, lse=self.lz)
+        ra.ring_attn_fwd(self.qz, self.kz, self.vz, True, P["N"], B=P["B"], layout="zigzag", o=self.oz, lse=self.lz,
+                         variant=RING_VARIANT[0])
         if e: e[2].record()
         # a2: restore token order
         ra.gather_rows(self.oz, self.restore, self.o)
@@ -721,6 +722,7 @@ def measure_varlen(ra, dev, reps=5):
 
 
 RING_DIST = dict(ranks=8)
+RING_VARIANT = [0]   # kernel variant of ra_ring_attn_fwd_ex (0: the library's choice)
 
 
 def measure_ring_dist(ra, wl, reps=3):
@@ -947,6 +949,8 @@ def main():
     ap.add_argument("--decode-requests", type=int, default=None, help="override the number of decode requests")
     ap.add_argument("--merge-tokens", type=int, default=None, help="override T of the stand-alone merge")
     ap.add_argument("--decode-split", type=int, default=None, help="override the decode's virtual blocks per split")
+    ap.add_argument("--ring-variant", type=int, default=None,
+                    help="bf16 kernel variant of the ring attention (ra_ring_attn_fwd_ex), for --parts runs")
     ap.add_argument("--cp-dist", action="store_true",
                     help="run the step split across the job's ranks (the path used for more than one GPU) even "
                          "on one rank")
@@ -955,6 +959,7 @@ def main():
     args = ap.parse_args()
     if args.parts == "all":
         for flag, val in (("--prefill-shape", args.prefill_shape), ("--prefill-seq", args.prefill_seq),
+                          ("--ring-variant", args.ring_variant),
                           ("--decode-requests", args.decode_requests), ("--merge-tokens", args.merge_tokens),
                           ("--decode-split", args.decode_split)):
             if val is not None:
@@ -964,6 +969,8 @@ def main():
         PREFILL.update(B=B, Hq=Hq, Hkv=Hkv, S=S, N=N)
     if args.prefill_seq:
         PREFILL["S"] = args.prefill_seq
+    if args.ring_variant is not None:
+        RING_VARIANT[0] = args.ring_variant
     if args.decode_requests:
         DECODE["R"] = args.decode_requests
     if args.merge_tokens:
