@@ -37,7 +37,8 @@ METRIC = "ring-attn fwd TFLOP/s (causal-adj) & % bf16 peak; decode+merge GB/s % 
 PREFILL = dict(B=1, Hq=32, Hkv=8, S=131072, d=128, N=16, seed=5)
 DECODE = dict(R=64, lo=4096, hi=131072, Hq=32, Hkv=8, d=128, bs=128, I=16, pcp=2, dcp=4, seed=4, split=16)
 # sources whose contents the recorded DRAM traffic of each kernel was measured on
-KERNEL_SOURCES = {"ring_attn_bf16": ["ra_attn_bf16.cu", "ra_attn_pair.cuh", "ra_attn_tc.cuh", "ra_sm100.cuh"],
+KERNEL_SOURCES = {"ring_attn_bf16": ["ra_attn_bf16.cu", "ra_attn_pair.cuh", "ra_ring_sched.cuh", "ra_attn_tc.cuh",
+                                     "ra_sm100.cuh"],
                   "cp_decode": ["ra_decode.cu"]}
 
 

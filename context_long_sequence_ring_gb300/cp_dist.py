@@ -63,8 +63,13 @@ class P2PExchange:
     the current stream, and ``wait`` makes the current stream wait for them: compute enqueued
     between ``start`` and ``wait`` overlaps the transfer."""
 
-    def __init__(self, group=None):
+    def __init__(self, group=None, timeout=None):
+        """``timeout`` (a datetime.timedelta) bounds each wait where the backend supports it
+        (gloo): a rank that never sends or receives then raises an error here instead of
+        leaving its neighbours waiting.  With NCCL the wait is a stream dependency and the
+        process group's own timeout applies."""
         self.group = group
+        self.timeout = timeout
         self.rank = dist.get_rank(group)
         self.world = dist.get_world_size(group)
 
@@ -78,10 +83,12 @@ class P2PExchange:
         ops += [dist.P2POp(dist.irecv, t, prv, self.group) for t in recv]
         return dist.batch_isend_irecv(ops)
 
-    @staticmethod
-    def wait(handle):
+    def wait(self, handle):
         for work in handle:
-            work.wait()
+            if self.timeout is None:
+                work.wait()
+            else:
+                work.wait(self.timeout)
 
 
 # ---------------------------------------------------------------------- prefill ring

@@ -155,6 +155,33 @@ def test_ring_attention_local_matches_full(N, causal):
         assert torch.equal(ks[r], keep[r])
 
 
+def _dropout_worker(rank, world, port, out):
+    # rank 1 initialises and then never joins the ring: rank 0 must get an error, not a hang
+    import datetime
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world, timeout=datetime.timedelta(seconds=20))
+    if rank == 1:
+        out[rank] = "left"
+        return
+    N, c = world, 2
+    q, k, v = _inputs(8, 1, 2 * N * c, 2, 1, 4)
+    idx = torch.as_tensor(_local_idx(N, c, rank))
+    ex = cp_dist.P2PExchange(timeout=datetime.timedelta(seconds=3))
+    try:
+        cp_dist.ring_attention(q[idx].contiguous(), k[idx].contiguous(), v[idx].contiguous(),
+                               step=_oracle_step(N, rank, True, 1), exchange=ex)
+        out[rank] = "finished"
+    except RuntimeError as e:
+        out[rank] = "error: " + str(e)[:80]
+
+
+def test_ring_detects_a_rank_that_never_joins():
+    out = mp.get_context("spawn").Manager().dict()
+    mp.start_processes(_dropout_worker, args=(2, _free_port(), out), nprocs=2, start_method="spawn")
+    assert out[1] == "left"
+    assert out[0].startswith("error"), out[0]
+
+
 # ---------------------------------------------------------------- decode merge over gloo ranks
 
 def _oracle_rescale(o_local, lse_all, w, o_scaled, lse_total):
