@@ -574,6 +574,7 @@ def run_ours(args, rank, world, dev):
     line["merge_stress"] = measure_merge(ra, dev)
     line["varlen_prefill"] = measure_varlen(ra, dev)
     line["cp_ring_emulated"] = measure_ring_dist(ra, wl)
+    line["cp_allgather_emulated"] = measure_allgather(ra, wl)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_rows)
     return line
@@ -627,6 +628,8 @@ def run_parts(args, dev):
         out["varlen"] = measure_varlen(ra, dev)
     if "ringdist" in parts:
         out["ringdist"] = measure_ring_dist(ra, wl)
+    if "allgather" in parts:
+        out["allgather"] = measure_allgather(ra, wl)
     print(json.dumps(out), flush=True)
 
 
@@ -763,6 +766,48 @@ def measure_ring_dist(ra, wl, reps=3):
     return {"ranks": N, "step_launches": N * N, "ms_all_ranks": round(ms, 3), "tflops": round(tf, 1),
             "frac_of_bf16_burst": round(tf / _peaks()["bf16"], 4),
             "note": "every rank's ring steps on one GPU, blocks rotated by device copies; not in value"}
+
+
+def measure_allgather(ra, wl, reps=2):
+    """The prefill in the form with the K/V all-gathered (the ranks' chunk pairs concatenated are the
+    gathered order), ranks emulated on this GPU: per rank, the restore of the gathered K/V to token
+    order (row-gather kernel) and its two chunks' attention over the keys in token order, in
+    32768-key segments (segmented prefill kernels).  All ranks run one after the other here."""
+    P = PREFILL
+    if "prefill" not in wl.parts or P["B"] != 1:
+        return None
+    N, S = RING_DIST["ranks"], P["S"]
+    c = S // (2 * N)
+    perm, restore = ra.zigzag_partition([S], N)
+    kz, vz = ra.gather_rows(wl.k, perm), ra.gather_rows(wl.v, perm)
+    qs = [ra.gather_rows(wl.q, perm[r * 2 * c:(r + 1) * 2 * c]) for r in range(N)]
+    k_nat, v_nat = torch.empty_like(kz), torch.empty_like(vz)
+    o = torch.empty_like(qs[0])
+    lse = torch.empty(qs[0].shape[:2], dtype=torch.float32, device=wl.dev)
+    attends = [ra.allgather_attend_fn(S, N, r, True) for r in range(N)]
+
+    def run():
+        for r in range(N):
+            ra.gather_rows(kz, restore, k_nat)
+            ra.gather_rows(vz, restore, v_nat)
+            attends[r](qs[r], k_nat, v_nat, o, lse)
+    run()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        run()
+    e1.record()
+    torch.cuda.synchronize()
+    if ra.device_status() != 0:
+        raise RuntimeError("device status after the all-gather prefill: %s" % ra.last_error())
+    ms = e0.elapsed_time(e1) / reps
+    tf = causal_flops(1, P["Hq"], S, P["d"]) / (ms * 1e-3) / 1e12
+    del qs, kz, vz, k_nat, v_nat
+    return {"ranks": N, "ms_all_ranks": round(ms, 3), "tflops": round(tf, 1),
+            "frac_of_bf16_burst": round(tf / _peaks()["bf16"], 4),
+            "note": "every rank's restore and attention on one GPU (the all-gather itself is communication); "
+                    "not in value"}
 
 
 MERGE = dict(P=8, T=32768, H=32, d=128, seed=7)
@@ -944,7 +989,8 @@ def main():
     ap.add_argument("--parts", default="all",
                     help="'all' for the benchmark line, else a comma list of 'prefill', 'decode', 'rope' (the "
                          "RoPE prologue, needs 'prefill'), 'reorg' (the KV reorg, needs 'decode'), 'merge', "
-                         "'segmented', 'varlen' and 'ringdist' (the ring across emulated devices, needs 'prefill') to run "
+                         "'segmented', 'varlen', 'ringdist' (the ring across emulated devices, needs 'prefill') and "
+                         "'allgather' (the all-gather-KV prefill across emulated devices, needs 'prefill') to run "
                          "only those parts (profiler captures)")
     ap.add_argument("--prefill-seq", type=int, default=None, help="override S of the prefill (multiple of 2N)")
     ap.add_argument("--decode-requests", type=int, default=None, help="override the number of decode requests")

@@ -198,6 +198,38 @@ def ring_attention_local(qs: Sequence[torch.Tensor], ks: Sequence[torch.Tensor],
     return list(zip(o_fin, lse))
 
 
+def allgather_kv_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, restore: torch.Tensor,
+                           gather: Callable[..., None], attend: Callable[..., None], group=None,
+                           out_dtype: Optional[torch.dtype] = None):
+    """Prefill with the K/V all-gathered instead of passed around a ring: the form the vLLM-Ascend
+    "Context Parallel (CP)" page says ships for PCP prefill (every device all-gathers the K/V of the
+    layer, attends its own queries over all of it, and drops the gathered K/V after use).
+
+      1. all-gather every rank's local K/V ([rows, Hkv, d], per sequence chunk r then chunk 2N-1-r):
+         the result is in the head-tail partition's gathered order;
+      2. ``gather(src, restore, dst)`` puts it back in token order with the partition's restore index
+         (pcp_allgather_restore_idx);
+      3. ``attend(q, k_nat, v_nat, o, lse)`` computes this rank's queries over the keys in token order.
+
+    Returns (O [rows, Hq, d] in out_dtype (default q's), LSE fp32 [rows, Hq]).
+    """
+    W = dist.get_world_size(group)
+    rows = k.shape[0]
+    k_all = torch.empty((W * rows,) + tuple(k.shape[1:]), dtype=k.dtype, device=k.device)
+    v_all = torch.empty_like(k_all)
+    dist.all_gather_into_tensor(k_all, k.contiguous(), group=group)
+    dist.all_gather_into_tensor(v_all, v.contiguous(), group=group)
+    k_nat = torch.empty((restore.numel(),) + tuple(k.shape[1:]), dtype=k.dtype, device=k.device)
+    v_nat = torch.empty_like(k_nat)
+    gather(k_all, restore, k_nat)
+    gather(v_all, restore, v_nat)
+    del k_all, v_all
+    o = torch.empty(q.shape, dtype=out_dtype or q.dtype, device=q.device)
+    lse = torch.empty(q.shape[:2], dtype=torch.float32, device=q.device)
+    attend(q, k_nat, v_nat, o, lse)
+    return o, lse
+
+
 # ---------------------------------------------------------------------- decode merge
 
 def cp_lse_ag_out_rs(o_local: torch.Tensor, lse_local: torch.Tensor, *, rescale: Callable[..., None],
@@ -230,3 +262,36 @@ def cp_lse_ag_out_rs(o_local: torch.Tensor, lse_local: torch.Tensor, *, rescale:
     out = torch.empty((R, Hq // W, d), dtype=torch.float32, device=o_local.device)
     dist.reduce_scatter_tensor(out, o_scaled.view(W * R, Hq // W, d), op=dist.ReduceOp.SUM, group=group)
     return out, lse_total
+
+
+def cp_lse_a2a(o_local: torch.Tensor, lse_local: torch.Tensor, *, split: Callable[..., None],
+               merge: Callable[..., None], group=None):
+    """The all-to-all form of the decode's merge across the ranks of ``group`` (vLLM-Ascend "Context
+    Parallel (CP)", DCP and PCP decode name it beside cp_lse_ag_out_rs): every rank holds its
+    partial O_w [R, Hq, d] (fp32, normalised over the keys it stores) and LSE_w [R, Hq].
+
+      1. ``split(o_local, lse_local, W, o_split, lse_split)`` lays them out by the rank that keeps
+         each head: o_split [W, R, Hq/W, d], lse_split [W, R, Hq/W];
+      2. an all-to-all sends slot v to rank v, which receives the W partials of its heads;
+      3. ``merge(o_parts, lse_parts, o, lse)`` merges them (the LSE merge over P = W).
+
+    Returns (O [R, Hq/W, d] fp32, LSE [R, Hq/W]) of this rank's heads, the same as
+    cp_lse_ag_out_rs.  Hq must be a multiple of the group size.
+    """
+    W = dist.get_world_size(group)
+    R, Hq, d = o_local.shape
+    if Hq % W != 0:
+        raise ValueError("Hq (%d) must be a multiple of the number of ranks (%d)" % (Hq, W))
+    hs = Hq // W
+    dev = o_local.device
+    o_split = torch.empty((W, R, hs, d), dtype=torch.float32, device=dev)
+    lse_split = torch.empty((W, R, hs), dtype=torch.float32, device=dev)
+    split(o_local, lse_local, W, o_split, lse_split)
+    o_parts = torch.empty_like(o_split)
+    lse_parts = torch.empty_like(lse_split)
+    dist.all_to_all_single(o_parts.view(W * R, hs, d), o_split.view(W * R, hs, d), group=group)
+    dist.all_to_all_single(lse_parts.view(W * R, hs), lse_split.view(W * R, hs), group=group)
+    o = torch.empty((R, hs, d), dtype=torch.float32, device=dev)
+    lse = torch.empty((R, hs), dtype=torch.float32, device=dev)
+    merge(o_parts, lse_parts, o, lse)
+    return o, lse

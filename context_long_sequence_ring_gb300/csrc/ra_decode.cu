@@ -547,6 +547,50 @@ __global__ void lse_rescale_kernel(const float* __restrict__ o_local, const floa
 }
 }  // namespace
 
+// The all-to-all form of the same merge: device w lays its output and LSE out by the device that
+// keeps each head, so that one all-to-all hands every device the W partials of its own heads
+// (merged there by ra_lse_merge).  One warp per (request, head) row.
+namespace {
+__global__ void head_split_kernel(const float* __restrict__ o_local, const float* __restrict__ lse_local, int W,
+                                  int64_t R, int Hq, int d, float* __restrict__ o_split,
+                                  float* __restrict__ lse_split) {
+  const int lane = threadIdx.x & 31;
+  const int64_t rows = R * Hq;
+  const int hs = Hq / W;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t row = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; row < rows;
+       row += nwarps) {
+    const int64_t r = row / Hq;
+    const int h = static_cast<int>(row % Hq);
+    const int v = h / hs, j = h % hs;
+    const int64_t at = (static_cast<int64_t>(v) * R + r) * hs + j;
+    const float lse = lse_local[row];
+    const bool live = lse != -CUDART_INF_F;
+    for (int e = 4 * lane; e < d; e += 128) {
+      const float4 a = live ? *reinterpret_cast<const float4*>(o_local + row * d + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+      *reinterpret_cast<float4*>(o_split + at * d + e) = a;
+    }
+    if (lane == 0) lse_split[at] = lse;
+  }
+}
+}  // namespace
+
+extern "C" ra_status ra_cp_head_split(const float* o_local, const float* lse_local, int32_t W, int64_t R, int32_t Hq,
+                                      int32_t d, float* o_split, float* lse_split, ra_stream stream) {
+  ra::clear_error();
+  RA_REQUIRE(W >= 1 && R >= 0 && Hq >= 1 && d >= 1, "W, Hq, d >= 1 and R >= 0");
+  RA_REQUIRE(Hq % W == 0, "Hq (%d) must be a multiple of W (%d)", Hq, W);
+  if (d % 4 != 0) return ra::fail(RA_ERR_UNSUPPORTED, "d must be a multiple of 4 (got %d)", d);
+  if (R == 0) return RA_OK;
+  RA_REQUIRE(o_local && lse_local && o_split && lse_split, "NULL pointer");
+  RA_REQUIRE(ra::aligned16(o_local) && ra::aligned16(o_split), "o_local and o_split must be 16-byte aligned");
+  const int64_t blocks = std::min<int64_t>(ra::ceil_div(R * Hq * 32, 256), 152 * 16);
+  head_split_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(o_local, lse_local, W, R, Hq, d, o_split,
+                                                                       lse_split);
+  RA_LAUNCH_CHECK("head_split_kernel");
+  return RA_OK;
+}
+
 extern "C" ra_status ra_cp_lse_rescale(const float* o_local, const float* lse_all, int32_t W, int32_t w, int64_t R,
                                        int32_t Hq, int32_t d, float* o_scaled, float* lse_total,
                                        ra_stream stream) {

@@ -56,6 +56,7 @@ SIGNATURES = {
     "ra_cp_decode_partials": [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
                               _i32, _i64, _f32, _i32, _vp, _vp, _c.POINTER(_i32), _vp],
     "ra_cp_lse_rescale": [_vp, _vp, _i32, _i32, _i64, _i32, _i32, _vp, _vp, _vp],
+    "ra_cp_head_split": [_vp, _vp, _i32, _i64, _i32, _i32, _vp, _vp, _vp],
     "ra_selftest_wait_timeout": [_i64, _vp],
     "ra_synth_fill": [_u64, _i64, _vp, _i32, _vp, _vp],
 }
@@ -280,24 +281,47 @@ def attn_block_fwd(q, k, v, q_pos0: int, k_pos0: int, causal: bool, scale: Optio
 
 
 def segmented_prefill_fwd(q, k, v, q_pos0: int, seg_tokens: int, causal: bool = True,
-                          scale: Optional[float] = None, out_dtype=torch.bfloat16, workspace=None):
+                          scale: Optional[float] = None, out_dtype=torch.bfloat16, workspace=None, o=None, lse=None):
     """Chunked prefill of q [Tq, Hq, d] (positions q_pos0..) over k/v [Tk, Hkv, d] (positions 0..) in
-    key segments of seg_tokens -> (O [Tq, Hq, d], LSE [Tq, Hq])."""
-    _need_cuda(q, k, v, workspace)
+    key segments of seg_tokens -> (O [Tq, Hq, d], LSE [Tq, Hq]).  O takes out_dtype, or the dtype of a
+    given ``o``."""
+    _need_cuda(q, k, v, workspace, o, lse)
     Tq, Hq, d = q.shape
     Tk, Hkv, _ = k.shape
     n = _sz(0)
     _check(lib().ra_segmented_prefill_workspace_size(Tq, Tk, Hq, d, seg_tokens, _c.byref(n)))
     if workspace is None:
         workspace = torch.empty(n.value, dtype=torch.uint8, device=q.device)
-    o = torch.empty((Tq, Hq, d), dtype=out_dtype, device=q.device)
-    lse = torch.empty((Tq, Hq), dtype=torch.float32, device=q.device)
+    if o is None:
+        o = torch.empty((Tq, Hq, d), dtype=out_dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty((Tq, Hq), dtype=torch.float32, device=q.device)
+    out_dtype = o.dtype
     _check(lib().ra_segmented_prefill_fwd(_ptr(q), _ptr(k), _ptr(v), Tq, Tk, Hq, Hkv, d, int(q_pos0),
                                           1 if causal else 0, float(scale or 0.0), seg_tokens, _ptr(o),
                                           RA_BF16 if out_dtype == torch.bfloat16 else RA_F32, _ptr(lse),
                                           _ptr(workspace), workspace.numel() * workspace.element_size(),
                                           _stream()))
     return o, lse
+
+
+def allgather_attend_fn(seq_len: int, n_ranks: int, rank: int, causal: bool = True, B: int = 1,
+                        seg_tokens: int = 32768, scale: Optional[float] = None):
+    """The attend callable of ``cp_dist.allgather_kv_attention`` for rank ``rank``: each of its local
+    chunks (per sequence chunk rank and chunk 2N-1-rank, c = seq_len/2N rows each) attends over the
+    sequence's keys in token order, in key segments of seg_tokens (ra_segmented_prefill_fwd), into
+    the rank's output rows."""
+    c = seq_len // (2 * n_ranks)
+
+    def attend(q, k_nat, v_nat, o, lse):
+        for b in range(B):
+            for half, ch in enumerate((rank, 2 * n_ranks - 1 - rank)):
+                rows = slice((b * 2 + half) * c, (b * 2 + half + 1) * c)
+                tk = (ch + 1) * c if causal else seq_len      # keys after the chunk are never visible
+                keys = slice(b * seq_len, b * seq_len + tk)
+                segmented_prefill_fwd(q[rows], k_nat[keys], v_nat[keys], ch * c, seg_tokens, causal, scale,
+                                      o=o[rows], lse=lse[rows])
+    return attend
 
 
 def lse_merge(o_parts, lse_parts, out_dtype=torch.float32, o=None, lse=None):
@@ -438,6 +462,34 @@ def cp_lse_rescale(o_local, lse_all, w: int, o_scaled=None, lse_total=None):
     _check(lib().ra_cp_lse_rescale(_ptr(o_local), _ptr(lse_all), W, w, R, Hq, d, _ptr(o_scaled), _ptr(lse_total),
                                    _stream()))
     return o_scaled, lse_total
+
+
+def cp_head_split(o_local, lse_local, W: int, o_split=None, lse_split=None):
+    """All-to-all form of the decode merge: o_local fp32 [R, Hq, d], lse_local [R, Hq] ->
+    (o_split [W, R, Hq/W, d], lse_split [W, R, Hq/W]) laid out by the device that keeps each head."""
+    _need_cuda(o_local, lse_local, o_split, lse_split)
+    R, Hq, d = o_local.shape
+    if o_split is None:
+        o_split = torch.empty((W, R, Hq // W, d), dtype=torch.float32, device=o_local.device)
+    if lse_split is None:
+        lse_split = torch.empty((W, R, Hq // W), dtype=torch.float32, device=o_local.device)
+    _check(lib().ra_cp_head_split(_ptr(o_local), _ptr(lse_local), W, R, Hq, d, _ptr(o_split), _ptr(lse_split),
+                                  _stream()))
+    return o_split, lse_split
+
+
+def cp_head_split_fn():
+    """The split callable of ``cp_dist.cp_lse_a2a``, on ra_cp_head_split."""
+    def split(o_local, lse_local, W, o_split, lse_split):
+        cp_head_split(o_local, lse_local, W, o_split, lse_split)
+    return split
+
+
+def lse_merge_fn(out_dtype=torch.float32):
+    """The merge callable of ``cp_dist.cp_lse_a2a``, on ra_lse_merge."""
+    def merge(o_parts, lse_parts, o, lse):
+        lse_merge(o_parts, lse_parts, out_dtype=out_dtype, o=o, lse=lse)
+    return merge
 
 
 def cp_lse_rescale_fn():

@@ -474,6 +474,26 @@ ra_status ra_cp_lse_rescale(const float* o_local, const float* lse_all, int32_t 
                             int32_t Hq, int32_t d, float* o_scaled, float* lse_total, ra_stream stream);
 
 /* ------------------------------------------------------------------------
+ * ra_cp_head_split -- the all-to-all form of the decode merge across W
+ * devices: device w lays out its output and LSE by the device that keeps each
+ * head, so that one all-to-all of o_split and lse_split hands every device the
+ * W partials of its own heads, which ra_lse_merge (P = W) then merges.
+ * Source: vLLM-Ascend "Context Parallel (CP)", DCP decode and PCP decode (the
+ * partial outputs and LSEs are exchanged by an all-to-all as an alternative to
+ * cp_lse_ag_out_rs).
+ *
+ * o_local   device float [R, Hq, d]: this device's output over its own keys.
+ * lse_local device float [R, Hq]: its LSE (-inf: no key; O is not read).
+ * o_split   device float [W, R, Hq/W, d] out: slot v holds heads
+ *           [v*Hq/W, (v+1)*Hq/W) of o_local (0 where the LSE is -inf).
+ * lse_split device float [W, R, Hq/W] out: the same heads' LSEs.
+ * Requires Hq % W == 0, d % 4 == 0 (RA_ERR_UNSUPPORTED otherwise), o_local and
+ * o_split 16-byte aligned.
+ * ---------------------------------------------------------------------- */
+ra_status ra_cp_head_split(const float* o_local, const float* lse_local, int32_t W, int64_t R, int32_t Hq,
+                           int32_t d, float* o_split, float* lse_split, ra_stream stream);
+
+/* ------------------------------------------------------------------------
  * ra_cp_decode_noalloc -- ra_cp_decode for callers that cannot allocate
  * device memory on the decode path (a runtime that reserves all device memory
  * at start-up and forbids allocation afterwards, an allocator that cannot

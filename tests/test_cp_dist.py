@@ -227,3 +227,83 @@ def test_cp_lse_ag_out_rs_over_gloo_ranks(world):
         assert out[r]["shape"] == (3, 8 // world, 6)
         assert out[r]["o_err"] < 1e-5 and out[r]["lse_err"] < 1e-5, out[r]
         assert out[r]["inf_ok"], out[r]
+
+
+# ---------------------------------------------------------------- prefill with the K/V all-gathered
+
+def _allgather_worker(rank, world, port, causal, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        N, c, Hq, Hkv, d = world, 3, 4, 2, 8
+        S = 2 * N * c
+        q, k, v = _inputs(9, 1, S, Hq, Hkv, d)
+        idx = torch.as_tensor(_local_idx(N, c, rank))
+        _, restore, _ = oracle.zigzag_partition([S], N)
+        got = {}
+
+        def gather(src, idx_, dst):                      # stand-in for the row-gather kernel
+            dst.copy_(src[idx_.long()])
+
+        def attend(ql, k_nat, v_nat, o, lse):           # stand-in for the attention kernel
+            got["k_nat"] = k_nat.clone()
+            O, L = oracle.attention_rows(ql, idx.numpy(), k_nat, v_nat, causal)
+            o.copy_(torch.from_numpy(O))
+            lse.copy_(torch.from_numpy(L))
+        o, lse = cp_dist.allgather_kv_attention(q[idx].contiguous(), k[idx].contiguous(), v[idx].contiguous(),
+                                                restore=torch.as_tensor(restore), gather=gather, attend=attend)
+        Of, Lf = oracle.full_attention(q, k, v, causal)
+        out[rank] = dict(k_restored=torch.equal(got["k_nat"], k), o_err=float(np.abs(o.numpy() - Of[idx]).max()),
+                         lse_err=float(np.abs(lse.numpy() - Lf[idx]).max()))
+    finally:
+        dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("world,causal", [(2, True), (4, True), (3, False)])
+def test_allgather_kv_prefill_over_gloo_ranks(world, causal):
+    out = mp.get_context("spawn").Manager().dict()
+    mp.start_processes(_allgather_worker, args=(world, _free_port(), causal, out), nprocs=world, start_method="spawn")
+    for r in range(world):
+        assert out[r]["k_restored"], "rank %d: gathered K not back in token order" % r
+        assert out[r]["o_err"] < 1e-12 and out[r]["lse_err"] < 1e-6, out[r]    # O in q's float64, LSE fp32
+
+
+# ---------------------------------------------------------------- decode merge by all-to-all
+
+def _oracle_split(o_local, lse_local, W, o_split, lse_split):
+    """Stand-in for the head-split kernel: heads of rank v into slot v."""
+    R, Hq, d = o_local.shape
+    hs = Hq // W
+    o_split.copy_(o_local.reshape(R, W, hs, d).permute(1, 0, 2, 3))
+    lse_split.copy_(lse_local.reshape(R, W, hs).permute(1, 0, 2))
+
+
+def _oracle_merge(o_parts, lse_parts, o, lse):
+    O, L = oracle.lse_merge(o_parts.double().numpy(), lse_parts.double().numpy())
+    o.copy_(torch.from_numpy(O))
+    lse.copy_(torch.from_numpy(L))
+
+
+def _a2a_worker(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        g = torch.Generator().manual_seed(12)
+        R, Hq, d = 3, 8, 6
+        o_all = torch.randn((world, R, Hq, d), generator=g, dtype=torch.float64)
+        l_all = torch.randn((world, R, Hq), generator=g, dtype=torch.float64) * 3
+        l_all[0, 1, 3] = -np.inf
+        o, lse = cp_dist.cp_lse_a2a(o_all[rank].float(), l_all[rank].float(), split=_oracle_split,
+                                    merge=_oracle_merge)
+        ref = oracle.cp_lse_ag_out_rs(list(o_all.numpy()), list(l_all.numpy()))[rank]
+        out[rank] = dict(o_err=float(np.abs(o.numpy() - ref[0]).max()), lse_err=float(np.abs(lse.numpy() - ref[1]).max()))
+    finally:
+        dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("world", [2, 4])
+def test_cp_lse_a2a_equals_ag_out_rs_over_gloo_ranks(world):
+    out = mp.get_context("spawn").Manager().dict()
+    mp.start_processes(_a2a_worker, args=(world, _free_port(), out), nprocs=world, start_method="spawn")
+    for r in range(world):
+        assert out[r]["o_err"] < 1e-5 and out[r]["lse_err"] < 1e-5, out[r]

@@ -143,3 +143,54 @@ def test_lse_rescale_against_the_oracle_collective(ra):
         got = parts[w][1].cpu().numpy()
         fin = np.isfinite(ref[w][1])
         assert np.array_equal(np.isfinite(got), fin) and np.abs(got[fin] - ref[w][1][fin]).max() <= 1e-5
+
+
+def test_a2a_merge_across_emulated_devices(ra):
+    # the all-to-all form: each rank lays out its partial by head owner (kernel), the all-to-all is
+    # emulated by handing slot v of every rank to rank v, and rank v merges W partials (kernel)
+    R, lo, hi, bs, I_, pcp, dcp, Hq, Hkv, d, split = 5, 1000, 9000, 128, 16, 2, 4, 32, 8, 128, 4
+    c = _case(ra, 65, R, lo, hi, bs, I_, pcp, dcp, Hq, Hkv, d)
+    qd = c["q"].to(DEV)
+    W = c["W"]
+    splits = []
+    for w in range(W):
+        op, lp = ra.cp_decode_partials(qd, c["kc"][w:w + 1].contiguous(), c["vc"][w:w + 1].contiguous(), c["bt"],
+                                       c["ctx"], I_, pcp, dcp, dev0=w, split_blocks=split)
+        ow, lw = ra.lse_merge(op, lp, out_dtype=torch.float32)
+        splits.append(ra.cp_head_split(ow, lw, W))
+    outs = []
+    for v in range(W):                                        # rank v receives slot v of every rank
+        o_parts = torch.stack([splits[w][0][v] for w in range(W)])
+        l_parts = torch.stack([splits[w][1][v] for w in range(W)])
+        outs.append(ra.lse_merge(o_parts, l_parts, out_dtype=torch.float32))
+    check_status(ra)
+    O = torch.cat([x[0] for x in outs], dim=1)
+    L = torch.cat([x[1] for x in outs], dim=1)
+    o_ref, l_ref = ra.cp_decode(qd, c["kc"], c["vc"], c["bt"], c["ctx"], I_, pcp, dcp, split_blocks=split,
+                                out_dtype=torch.float32)
+    assert (O - o_ref).abs().max().item() <= 1e-5 and (L - l_ref).abs().max().item() <= 1e-5
+    tol = TOL[torch.bfloat16]
+    for r in range(R):
+        s0, s1 = int(c["qsl"][r]), int(c["qsl"][r + 1])
+        Or, Lr = oracle.decode_reference(c["q"][r], c["kt"][s0:s1], c["vt"][s0:s1])
+        assert np.abs(O[r].cpu().numpy() - Or).max() <= tol["o_max"]
+        assert np.abs(L[r].cpu().numpy() - Lr).max() <= tol["lse"]
+
+
+def test_head_split_layout_and_empty_rows(ra):
+    W, R, Hq, d = 4, 3, 8, 64
+    g = torch.Generator().manual_seed(66)
+    o = torch.randn((R, Hq, d), generator=g)
+    lse = torch.randn((R, Hq), generator=g)
+    lse[1, 5] = -float("inf")
+    o[1, 5] = float("nan")                                     # not read: its LSE is -inf
+    os_, ls_ = ra.cp_head_split(o.to(DEV), lse.to(DEV), W)
+    check_status(ra)
+    hs = Hq // W
+    for v in range(W):
+        for j in range(hs):
+            h = v * hs + j
+            assert torch.equal(ls_[v, :, j].cpu(), lse[:, h])
+            want = o[:, h].clone()
+            want[~torch.isfinite(lse[:, h])] = 0.0
+            assert torch.equal(os_[v, :, j].cpu(), want)

@@ -190,3 +190,28 @@ def test_ring_over_eight_ranks_at_full_size(ra):
         O, L = oracle.attention_rows(qr, rows, kk[:rows.max() + 1], vv[:rows.max() + 1], True)
         sel = torch.as_tensor(loc, device=DEV)
         assert_parity(res[r][0][sel], O, res[r][1][sel], L, torch.bfloat16, "rank %d sampled rows" % r)
+
+
+@pytest.mark.parametrize("N,c,Hq,Hkv,causal,seg", [(4, 256, 4, 2, True, 512), (3, 200, 3, 1, True, 4096),
+                                                   (2, 384, 4, 4, False, 700)])
+def test_allgather_kv_prefill_emulated(ra, N, c, Hq, Hkv, causal, seg):
+    # each rank's K/V all-gathered (emulated by concatenation, which is the gathered order), put back
+    # in token order by the row-gather kernel with the partition's restore index, then the rank's two
+    # chunks attend over the keys in token order in segments of `seg` keys
+    d = 128
+    S = 2 * N * c
+    q, k, v = _host_inputs(53, 1, S, Hq, Hkv, d)
+    perm, restore = ra.zigzag_partition([S], N)
+    idx = [torch.as_tensor(_local_idx(N, c, r)) for r in range(N)]
+    k_all = torch.cat([k[i] for i in idx]).to(DEV)
+    v_all = torch.cat([v[i] for i in idx]).to(DEV)
+    k_nat, v_nat = ra.gather_rows(k_all, restore), ra.gather_rows(v_all, restore)
+    assert torch.equal(k_nat.cpu(), k)
+    O, L = oracle.full_attention(q, k, v, causal)
+    for r in range(N):
+        ql = q[idx[r]].contiguous().to(DEV)
+        o = torch.empty(ql.shape, dtype=torch.bfloat16, device=DEV)
+        lse = torch.empty(ql.shape[:2], dtype=torch.float32, device=DEV)
+        ra.allgather_attend_fn(S, N, r, causal, seg_tokens=seg)(ql, k_nat, v_nat, o, lse)
+        check_status(ra)
+        assert_parity(o, O[idx[r]], lse, L[idx[r]], torch.bfloat16, "rank %d" % r)
