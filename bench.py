@@ -12,6 +12,13 @@ Prints one JSON line.  ``value`` is causal-adjusted attention TFLOP/s over the
 whole timed step (prefill + decode); the decode+merge GB/s and the per-kernel
 rooflines are reported beside it.  ``--impl reference`` times the float64
 oracle instead (a bounded sample per step on the host cores).
+
+On one GPU the step runs the single-device kernels.  Under torchrun with N > 1
+ranks (or with --cp-dist) the same step is split across the ranks: the prefill
+as a ring of N ranks, each holding its head-tail chunk pair and passing K/V
+blocks to the next over NCCL, and the decode with the cache's devices spread
+over the ranks and merged by cp_lse_ag_out_rs (strong scaling: the work is the
+same at every N).
 """
 
 from __future__ import annotations
@@ -466,6 +473,8 @@ def run_dist(args, rank, world, dev):
 
 
 def run_ours(args, rank, world, dev):
+    """The benchmark line on one GPU: the single-device kernels (the ring of N virtual ranks in one
+    launch, the decode over all W cache devices with one merge).  More ranks run run_dist."""
     from context_long_sequence_ring_gb300 import ringattn as ra
     ra.lib()
     wl = Workload(ra, dev)
@@ -503,7 +512,7 @@ def run_ours(args, rank, world, dev):
     dec_bytes, kv_bytes = wl.decode_bytes()
     pk = _peaks()
     ms_step = ms_total / args.steps
-    value = world * flops / (ms_step * 1e-3) / 1e12
+    value = flops / (ms_step * 1e-3) / 1e12
 
     # e2e through the public API from pinned host buffers: H2D Q/K/V and the decode step's
     # inputs, the full step, D2H of O/LSE and the decode output.
@@ -540,13 +549,13 @@ def run_ours(args, rank, world, dev):
     dec_gbs = dec_bytes / (decode_kernel_ms * 1e-3) / 1e9
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(ms_step, 3), "higher_is_better": True, "scaling": "weak",
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 3), "higher_is_better": True, "scaling": "strong",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded counter-based N(0,1), bf16)",
         "config": {"workload": workload_name(),
                    "prefill": PREFILL, "decode": {k: v for k, v in DECODE.items()},
                    "l2": "inputs larger than L2 (Q 1 GiB, K/V 256 MiB each, KV cache %.1f GB)" % (
                        2 * wl.kc.numel() * 2 / 1e9),
-                   "parallelism": "replicas (one independent problem per GPU)" if world > 1 else "1 GPU"},
+                   "parallelism": "1 GPU (N virtual context-parallel ranks in one kernel)"},
         "parts": {
             "prefill_ms": round(prefill_ms, 3), "ring_attn_kernel_ms": round(attn_ms, 3),
             "ring_attn_tflops": round(attn_tflops, 1),
@@ -560,10 +569,10 @@ def run_ours(args, rank, world, dev):
                             "frac": round(dec_gbs / pk["hbm"], 4), "traffic": _traffic("cp_decode"),
                             "kernel": "cp_decode_kernel + lse_merge_kernel", "peak_kind": "HBM copy (%s)" % pk["src"],
                             "algorithmic": "%d bytes per step" % dec_bytes},
-        "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+        "e2e": {"value": round(flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3),
                 "copies": "pipelined on two copy streams, double-buffered step inputs and outputs",
-                "serial": {"value": round(world * flops / (serial_ms * 1e-3) / 1e12, 2),
+                "serial": {"value": round(flops / (serial_ms * 1e-3) / 1e12, 2),
                            "ms_per_step": round(serial_ms, 3)}},
         "gpu_launches": wl.launches_per_step * args.steps,
         "clocks": clk.summary(),
@@ -956,7 +965,7 @@ def run_reference(args):
                     "is not timed" % args.cpu_rows}
     return {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 2),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "higher_is_better": True, "scaling": "strong", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": workload_name(), "prefill": PREFILL, "decode": {k: v for k, v in DECODE.items()},
                        "sample": "prefill query rows sampled at random, rate extrapolated to the whole step"},
             "cpu_baseline": cb,

@@ -437,7 +437,8 @@ ra_status ra_cp_decode(const void* q, const void* k_cache, const void* v_cache,
  *             (s+1)*split_blocks), O normalised by its own sum.  A partial
  *             with no token has LSE -inf and its O is not written.
  * n_parts_out host int32 out (may be NULL): P.  With o_parts and lse_parts
- *             both NULL only P is returned and nothing is launched.
+ *             both NULL only P is returned and nothing is launched (the
+ *             other arguments are checked as for a launch).
  * Errors: as ra_cp_decode; [dev0, dev0+n_dev) outside [0, W) is
  * RA_ERR_INVALID_ARG.
  * ---------------------------------------------------------------------- */

@@ -1,4 +1,4 @@
-"""Host-side logic of bench.py at N > 1 (replicas with a barrier and a max over
+"""Host-side logic of bench.py at N > 1 (the barrier and the max over
 ranks), run as two gloo ranks on the CPU."""
 import os
 import socket
