@@ -156,3 +156,29 @@ def test_product_path_has_no_oracle_or_fallback():
     for f in glob.glob(os.path.join(pkg, "*.py")) + glob.glob(os.path.join(pkg, "csrc", "*")):
         src = open(f).read()
         assert "import oracle" not in src and "from oracle" not in src, f
+
+
+def test_cross_device_entry_points_validate_on_the_host(ra):
+    p = ctypes.c_void_p(16)   # never dereferenced: validation fails, or only sizes are returned, first
+    # ring step: rank/src outside [0, N), o_in without lse_in, a bf16 output over the fp32 running one
+    step = lambda **kw: _call(ra, "ra_ring_step_fwd", p, p, p, 1, kw.get("Hq", 4), 2, 128, kw.get("d", 128), 2,
+                              kw.get("rank", 0), kw.get("src", 1), 1, 0.0, kw.get("o_in", None),
+                              kw.get("lse_in", None), kw.get("o_out", p), kw.get("dt", 0), p, None)
+    assert step(rank=2) == ra.RA_ERR_INVALID_ARG and "rank" in ra.last_error()
+    assert step(src=-1) == ra.RA_ERR_INVALID_ARG
+    assert step(Hq=3) == ra.RA_ERR_INVALID_ARG and "multiple of Hkv" in ra.last_error()
+    assert step(o_in=p) == ra.RA_ERR_INVALID_ARG and "together" in ra.last_error()
+    assert step(o_in=p, lse_in=p, o_out=p, dt=1) == ra.RA_ERR_INVALID_ARG and "in place" in ra.last_error()
+    assert step(d=96) == ra.RA_ERR_UNSUPPORTED
+    # decode partials: the device range must lie in [0, pcp*dcp); NULL outputs return the count only
+    P = ctypes.c_int32(0)
+    part = lambda dev0, n_dev, out=None: _call(ra, "ra_cp_decode_partials", p, p, p, p, p, 3, 32, 8, 128, 128, 16, 2,
+                                               4, dev0, n_dev, 33, 64, 0.0, 8, out, out, ctypes.byref(P), None)
+    assert part(6, 3) == ra.RA_ERR_INVALID_ARG and "devices" in ra.last_error()
+    assert part(2, 3) == ra.RA_OK and P.value == 3 * 5        # 3 devices x ceil(33/8) splits
+    # rescale and head split: heads must divide over the devices
+    assert _call(ra, "ra_cp_lse_rescale", p, p, 3, 0, 4, 32, 128, p, p, None) == ra.RA_ERR_INVALID_ARG
+    assert _call(ra, "ra_cp_lse_rescale", p, p, 4, 4, 4, 32, 128, p, p, None) == ra.RA_ERR_INVALID_ARG
+    assert _call(ra, "ra_cp_lse_rescale", p, p, 4, 1, 0, 32, 128, p, p, None) == ra.RA_OK      # R = 0: nothing to do
+    assert _call(ra, "ra_cp_head_split", p, p, 3, 4, 32, 128, p, p, None) == ra.RA_ERR_INVALID_ARG
+    assert _call(ra, "ra_cp_head_split", p, p, 4, 4, 32, 6, p, p, None) == ra.RA_ERR_UNSUPPORTED
