@@ -215,3 +215,32 @@ def test_allgather_kv_prefill_emulated(ra, N, c, Hq, Hkv, causal, seg):
         ra.allgather_attend_fn(S, N, r, causal, seg_tokens=seg)(ql, k_nat, v_nat, o, lse)
         check_status(ra)
         assert_parity(o, O[idx[r]], lse, L[idx[r]], torch.bfloat16, "rank %d" % r)
+
+
+def test_allgather_kv_prefill_at_full_size(ra):
+    """The S=131072, Hq=32, Hkv=8 prefill in the all-gather form over 8 emulated ranks (32768-key
+    segments): every output of ranks 0, 3 and 7 equals the single-device ring kernel's to the bf16
+    tolerance."""
+    S, Hq, Hkv, d, N, seed = 131072, 32, 8, 128, 8, 5
+    tab = I.normal_table(torch.bfloat16)
+    q = ra.synth_fill(I.tensor_key(seed, I.TID_Q), tab, (S, Hq, d))
+    k = ra.synth_fill(I.tensor_key(seed, I.TID_K), tab, (S, Hkv, d))
+    v = ra.synth_fill(I.tensor_key(seed, I.TID_V), tab, (S, Hkv, d))
+    o_ref, lse_ref = ra.ring_attn_fwd(q, k, v, True, 16)
+    perm, restore = ra.zigzag_partition([S], N)
+    kz, vz = ra.gather_rows(k, perm), ra.gather_rows(v, perm)          # what the all-gather delivers
+    k_nat, v_nat = ra.gather_rows(kz, restore), ra.gather_rows(vz, restore)
+    assert torch.equal(k_nat, k) and torch.equal(v_nat, v)
+    c = S // (2 * N)
+    tol = TOL[torch.bfloat16]
+    for r in (0, 3, N - 1):
+        rows = perm[r * 2 * c:(r + 1) * 2 * c]
+        ql = ra.gather_rows(q, rows)
+        o = torch.empty(ql.shape, dtype=torch.bfloat16, device=DEV)
+        lse = torch.empty(ql.shape[:2], dtype=torch.float32, device=DEV)
+        ra.allgather_attend_fn(S, N, r, True)(ql, k_nat, v_nat, o, lse)
+        check_status(ra)
+        ro, rl = o_ref[rows.long()], lse_ref[rows.long()]
+        e = (o.float() - ro.float()).abs()
+        assert e.max().item() <= tol["o_max"] and e.mean().item() <= tol["o_mean"] / 4, (r, e.max().item())
+        assert (lse - rl).abs().max().item() <= tol["lse"]
