@@ -194,3 +194,51 @@ def test_head_split_layout_and_empty_rows(ra):
             want = o[:, h].clone()
             want[~torch.isfinite(lse[:, h])] = 0.0
             assert torch.equal(os_[v, :, j].cpu(), want)
+
+
+def test_dcp_merge_at_full_decode_size(ra):
+    """The 64-request decode workload (contexts U[4096, 131072], Hq=32, Hkv=8, block 128, interleave
+    16, pcp=2, dcp=4) with each of the 8 cache devices as its own rank: partials, local merge,
+    cp_lse_ag_out_rs with the rescale kernel (all-gather and reduce-scatter emulated), against
+    ra_cp_decode on the same cache, and sampled requests against plain attention."""
+    R, lo, hi, bs, I_, pcp, dcp, Hq, Hkv, d, split, seed = 64, 4096, 131072, 128, 16, 2, 4, 32, 8, 128, 16, 4
+    W = pcp * dcp
+    wl = I.decode_workload(seed, R, lo, hi, bs, pcp, dcp)
+    T = wl["total_tokens"]
+    tab = I.normal_table(torch.bfloat16)
+    kt = ra.synth_fill(I.tensor_key(seed, I.TID_K), tab, (T, Hkv, d))
+    vt = ra.synth_fill(I.tensor_key(seed, I.TID_V), tab, (T, Hkv, d))
+    ctx = wl["ctx_lens"]
+    qsl = torch.zeros(R + 1, dtype=torch.int32)
+    qsl[1:] = torch.cumsum(ctx, 0)
+    pos = torch.cat([torch.arange(int(L), dtype=torch.int32) for L in ctx])
+    bt = wl["block_table"].to(DEV)
+    slot = ra.cp_slot_mapping(qsl.to(DEV), pos.to(DEV), bt, bs, I_, pcp, dcp)
+    kc = torch.empty((W, wl["num_blocks"], Hkv, bs, d), dtype=torch.bfloat16, device=DEV)
+    vc = torch.empty_like(kc)
+    ra.cp_kv_scatter(kt, vt, slot, kc, vc)
+    del slot
+    q = I.synth_normal(seed, I.TID_Q, (R, Hq, d), torch.bfloat16)
+    qd, ctx_d = q.to(DEV), ctx.to(DEV)
+    outs = []
+    for w in range(W):
+        op, lp = ra.cp_decode_partials(qd, kc[w:w + 1], vc[w:w + 1], bt, ctx_d, I_, pcp, dcp, dev0=w,
+                                       split_blocks=split)
+        outs.append(ra.lse_merge(op, lp, out_dtype=torch.float32))
+    lse_all = torch.stack([x[1] for x in outs])
+    scaled = [ra.cp_lse_rescale(outs[w][0], lse_all, w) for w in range(W)]
+    total = torch.stack([s_[0] for s_ in scaled]).sum(0)
+    O = torch.cat([total[w] for w in range(W)], dim=1)
+    L = torch.cat([s_[1] for s_ in scaled], dim=1)
+    check_status(ra)
+    o_ref, l_ref = ra.cp_decode(qd, kc, vc, bt, ctx_d, I_, pcp, dcp, split_blocks=split, out_dtype=torch.float32)
+    assert (O - o_ref).abs().max().item() <= 1e-5 and (L - l_ref).abs().max().item() <= 1e-5
+    tol = TOL[torch.bfloat16]
+    for r in (0, 17, 63):
+        s0, s1 = int(qsl[r]), int(qsl[r + 1])
+        toks = np.arange(s0, s1)          # the oracle's K/V from the host generator
+        kr = I.synth_rows(seed, I.TID_K, toks, Hkv * d, torch.bfloat16).reshape(s1 - s0, Hkv, d)
+        vr = I.synth_rows(seed, I.TID_V, toks, Hkv * d, torch.bfloat16).reshape(s1 - s0, Hkv, d)
+        Or, Lr = oracle.decode_reference(q[r], kr, vr)
+        assert np.abs(O[r].cpu().numpy() - Or).max() <= tol["o_max"]
+        assert np.abs(L[r].cpu().numpy() - Lr).max() <= tol["lse"]
