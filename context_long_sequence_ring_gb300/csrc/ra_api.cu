@@ -48,9 +48,11 @@ extern "C" ra_status ra_device_status(ra_stream stream) {
                           ra::fetch_error_attn_f32, ra::fetch_error_attn_bf16, ra::fetch_error_attn_block,
                           ra::fetch_error_rope, ra::fetch_error_ring_step};
   const char* names[] = {"partition/gather", "kv cache", "decode/merge", "attention fp32",
-                         "ring attention bf16", "block attention bf16", "rope gather"};
+                         "ring attention bf16", "block attention bf16", "rope gather", "ring step"};
+  static_assert(sizeof(fetch) / sizeof(fetch[0]) == sizeof(names) / sizeof(names[0]),
+                "one name per module error word");
   ra_status first = RA_OK;
-  for (int i = 0; i < 7; ++i) {
+  for (size_t i = 0; i < sizeof(fetch) / sizeof(fetch[0]); ++i) {
     int where = 0;
     int s = fetch[i](&where);
     if (s < 0) return ra::fail(RA_ERR_CUDA, "reading the device error word failed");

@@ -124,8 +124,9 @@ __global__ void __launch_bounds__(kThreads2, 1)
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
       uint32_t kv_cnt = 0;
-      bool issued[STAGES] = {false, false};
-      uint32_t last_ph[STAGES] = {0, 0};
+      // copies issued so far (stage phase of the last one), awaited before an aborted CTA exits
+      bool q_iss = false, k_iss[STAGES] = {false, false}, v_iss[STAGES] = {false, false};
+      uint32_t q_ph = 0, k_ph[STAGES] = {0, 0}, v_ph[STAGES] = {0, 0};
       bool ok = true;
       for (int ti = 0; ti < n_tiles && ok; ++ti) {
         pol.set_tile(ti);
@@ -137,6 +138,8 @@ __global__ void __launch_bounds__(kThreads2, 1)
           for (int s = 0; s < SLABS; ++s)
             tma_load_3d(smem_u32(sm.q[h] + s * BM * 128), &tmQ, qb, 64 * s, pol.q_head(h), qrow);
         }
+        q_iss = true;
+        q_ph = ti & 1;
         typename Pol::KvPos kp;
         pol.kv_begin(kp);
         while (pol.kv_next(kp)) {
@@ -147,21 +150,24 @@ __global__ void __launch_bounds__(kThreads2, 1)
           mbar_arrive_expect_tx(smem_u32(&sm.k_full[st]), kTileBytes);
           for (int s = 0; s < SLABS; ++s)
             tma_load_3d(smem_u32(sm.k[st] + s * BN * 128), &tmK, smem_u32(&sm.k_full[st]), 64 * s, pol.kvh(), krow);
+          k_iss[st] = true;
+          k_ph[st] = ph;
           if (!(ok = mbar_wait(smem_u32(&sm.v_empty[st]), ph ^ 1, abort_flag, lim, 103))) break;
           mbar_arrive_expect_tx(smem_u32(&sm.v_full[st]), kTileBytes);
           for (int s = 0; s < SLABS; ++s)
             tma_load_3d(smem_u32(sm.v[st] + s * BN * 128), &tmV, smem_u32(&sm.v_full[st]), 64 * s, pol.kvh(), krow);
-          issued[st] = true;
-          last_ph[st] = ph;
+          v_iss[st] = true;
+          v_ph[st] = ph;
           ++kv_cnt;
         }
       }
       if (!ok) {
-        for (int s = 0; s < STAGES; ++s)
-          if (issued[s]) {
-            mbar_wait(smem_u32(&sm.k_full[s]), last_ph[s], abort_flag, 1 << 22, 0);
-            mbar_wait(smem_u32(&sm.v_full[s]), last_ph[s], abort_flag, 1 << 22, 0);
-          }
+        // let the copies already in flight land before the CTA exits
+        if (q_iss) mbar_wait_quiesce(smem_u32(&sm.q_full), q_ph, 1 << 22);
+        for (int s = 0; s < STAGES; ++s) {
+          if (k_iss[s]) mbar_wait_quiesce(smem_u32(&sm.k_full[s]), k_ph[s], 1 << 22);
+          if (v_iss[s]) mbar_wait_quiesce(smem_u32(&sm.v_full[s]), v_ph[s], 1 << 22);
+        }
       }
     }
   } else if (warp == 1) {
@@ -239,7 +245,10 @@ __global__ void __launch_bounds__(kThreads2, 1)
         kv_cnt += nkv;
       }
       mma_commit(smem_u32(&sm.drain));
-      mbar_wait(smem_u32(&sm.drain), 0, abort_flag, ok ? lim : (1 << 22), 118);
+      if (!mbar_wait_quiesce(smem_u32(&sm.drain), 0, ok ? lim : (1 << 22)) && ok) {
+        *abort_flag = 1;
+        ra_record_error(RA_ERR_TIMEOUT, 118);
+      }
     }
   } else if (warp >= 4) {
     // ============================================================ softmax + epilogue (head h)

@@ -65,6 +65,17 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// Bounded wait on the way out of a kernel: for this thread's own copies or
+// MMAs to land before the CTA frees tensor memory or exits.  Unlike mbar_wait
+// it does not stop at the abort flag (which may already be raised); it gives
+// up after `limit` cycles and returns false.
+__device__ __forceinline__ bool mbar_wait_quiesce(uint32_t bar, uint32_t parity, long long limit) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity))
+    if (clock64() - t0 > limit) return false;
+  return true;
+}
+
 // ------------------------------------------------------------------ TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
