@@ -180,11 +180,15 @@ __global__ void __launch_bounds__(kThreads2, 1)
       const uint64_t dk[STAGES] = {desc_sw128(smem_u32(sm.k[0]), 16, 1024), desc_sw128(smem_u32(sm.k[1]), 16, 1024)};
       const uint64_t dv[STAGES] = {desc_sw128(smem_u32(sm.v[0]), BN * 128, 1024),
                                    desc_sw128(smem_u32(sm.v[1]), BN * 128, 1024)};
+      // Whether slot 1's P is known to be ready: tested while the last score MMAs of slot 0 are still
+      // queued, so that the barrier check overlaps tensor work instead of following it.
+      bool p1_ready = false;
       auto issue_s = [&](int h, int st) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off16 = ((kk >> 2) * (BM * 128) + (kk & 3) * 32) >> 4;
           mma_bf16_ss(tmem + h * BN, dq[h] + off16, dk[st] + off16, kIdescS, kk > 0 ? 1u : 0u);
+          if (h == 0 && kk == D / 16 - 3) p1_ready = mbar_test_wait(smem_u32(&sm.p_full[1]), pf_cnt[1] & 1);
         }
         mma_commit(smem_u32(&sm.s_full[h]));
       };
@@ -216,23 +220,22 @@ __global__ void __launch_bounds__(kThreads2, 1)
           const bool more = j + 1 < nkv;
           const int st1 = (c + 1) % STAGES;
           const uint32_t ph1 = ((c + 1) / STAGES) & 1;
-          // O_0 += P_0 V_j
+          // The waits that do not depend on the softmax come first, while slot 0's P is still being
+          // made: after P_0 lands nothing but the MMAs stands between it and the tensor core.
+          if (!(ok = mbar_wait(smem_u32(&sm.v_full[st]), ph, abort_flag, lim, 113))) break;
+          if (more && !(ok = mbar_wait(smem_u32(&sm.k_full[st1]), ph1, abort_flag, lim, 115))) break;
+          if (j == 0 && !(ok = mbar_wait(smem_u32(&sm.o_empty[0]), (ti & 1) ^ 1, abort_flag, lim, 114))) break;
+          if (j == 0 && !(ok = mbar_wait(smem_u32(&sm.o_empty[1]), (ti & 1) ^ 1, abort_flag, lim, 117))) break;
+          // O_0 += P_0 V_j, then S_0 of tile j+1
           if (!(ok = mbar_wait(smem_u32(&sm.p_full[0]), pf_cnt[0] & 1, abort_flag, lim, 112))) break;
           ++pf_cnt[0];
-          if (!(ok = mbar_wait(smem_u32(&sm.v_full[st]), ph, abort_flag, lim, 113))) break;
-          if (j == 0 && !(ok = mbar_wait(smem_u32(&sm.o_empty[0]), (ti & 1) ^ 1, abort_flag, lim, 114))) break;
           tc_fence_after();
           issue_pv(0, st, j == 0);
-          // S_0 of tile j+1
-          if (more) {
-            if (!(ok = mbar_wait(smem_u32(&sm.k_full[st1]), ph1, abort_flag, lim, 115))) break;
-            tc_fence_after();
-            issue_s(0, st1);
-          }
+          p1_ready = false;
+          if (more) issue_s(0, st1);
           // O_1 += P_1 V_j
-          if (!(ok = mbar_wait(smem_u32(&sm.p_full[1]), pf_cnt[1] & 1, abort_flag, lim, 116))) break;
+          if (!p1_ready && !(ok = mbar_wait(smem_u32(&sm.p_full[1]), pf_cnt[1] & 1, abort_flag, lim, 116))) break;
           ++pf_cnt[1];
-          if (j == 0 && !(ok = mbar_wait(smem_u32(&sm.o_empty[1]), (ti & 1) ^ 1, abort_flag, lim, 117))) break;
           tc_fence_after();
           issue_pv(1, st, j == 0);
           mma_commit(smem_u32(&sm.v_empty[st]));
