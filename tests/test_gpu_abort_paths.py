@@ -1,7 +1,8 @@
 """Failure detection of the tcgen05 kernels through their real abort path.
 
 A child process runs with RA_WAIT_LIMIT_CYCLES=64, so the first wait of every
-tensor-core kernel that is not satisfied at once expires.  Each kernel must
+tensor-core kernel that is not satisfied at once expires: the ring kernel in its
+three variants and its several-request form, the ring step and the block kernel.  Each kernel must
 then record RA_ERR_TIMEOUT in its own module's error word, let its copies and
 MMAs in flight land, free tensor memory and return; ra_device_status() must
 report the error with the module's name, and the context must stay usable for
@@ -29,10 +30,17 @@ out = {}
 def status(name):
     st = ra.device_status()
     out[name] = [int(st), ra.last_error() if st else ""]
-# ring-order attention (two-head pipeline)
+# ring-order attention: the two-head pipeline, the one-head kernel, the adjacent-tile schedule
 q, k, v = rnd(1024, 4, 128), rnd(1024, 2, 128), rnd(1024, 2, 128)
 ra.ring_attn_fwd(q, k, v, True, 2)
 status("ring")
+ra.ring_attn_fwd(q, k, v, True, 2, variant=1)
+status("ring_one_head")
+ra.ring_attn_fwd(q, k, v, True, 2, variant=3)
+status("ring_tiles")
+# several requests in one call (rows of the gathered layout: 640 + 384)
+ra.ring_attn_fwd_varlen(q, k, v, [640, 384], True, 2)
+status("varlen")
 # one rank's ring step (the across-devices kernel)
 ra.ring_step_fwd(q[:512], k[:512], v[:512], 2, 0, 0, True)
 status("ring_step")
@@ -61,8 +69,9 @@ def test_timeouts_are_reported_per_module_and_context_survives():
     res = json.loads(r.stdout.strip().splitlines()[-1])
     from context_long_sequence_ring_gb300 import ringattn as ra
 
-    for name, module in (("ring", "ring attention bf16"), ("ring_step", "ring step"),
-                         ("block", "block attention bf16")):
+    for name, module in (("ring", "ring attention bf16"), ("ring_one_head", "ring attention bf16"),
+                         ("ring_tiles", "ring attention bf16"), ("varlen", "ring attention bf16"),
+                         ("ring_step", "ring step"), ("block", "block attention bf16")):
         st, msg = res[name]
         assert st == ra.RA_ERR_TIMEOUT, (name, st, msg)
         assert module in msg, (name, msg)
